@@ -1,0 +1,214 @@
+/*
+ * pa.h - C ABI of the paged KV-cache hot path for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the PagedAttention serving scheme:
+ *   - "Efficient Memory Management for Large Language Model Serving with PagedAttention"
+ *     (paper summary page), paragraphs on the PagedAttention kernel, the block table,
+ *     copy-on-write sharing and all-or-nothing preemption;
+ *   - "When KV Capacity Runs Out: Pausing and Resuming Requests", Figures 1, 2 and 4;
+ *   - "KV Cache Preemption in vLLM", section "Swap versus recompute";
+ *   - "41 · Preemption, Recomputation & KV Pressure", section 3 (swap).
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * Memory.    Every buffer is owned by the caller. Pointers documented as "device" must be
+ *            device memory of the current CUDA device; "host" pointers are ordinary host
+ *            memory read synchronously during the call; "pinned host" pointers must come
+ *            from cudaHostAlloc / cudaHostRegister (e.g. torch pin_memory()). The library
+ *            allocates and frees nothing.
+ * Ordering.  Every call only enqueues work on `stream` (a cudaStream_t; NULL = legacy
+ *            default stream) and returns; nothing blocks on the device. Results are
+ *            visible to later work on the same stream.
+ * Errors.    Host-side validation failures return PA_EINVAL (bad pointer, size, alignment,
+ *            layout) or PA_EUNSUPPORTED (a valid combination this build has no kernel for)
+ *            and enqueue nothing. A failed launch returns PA_ECUDA. pa_last_error_message()
+ *            describes the latest non-OK status of the calling thread.
+ *            Indices that live in device memory (block tables, slot mappings, copy pairs,
+ *            context lengths) are checked on the device: a bad index is skipped and the
+ *            matching PA_ERR_* bit is OR-ed into *err_flag (a device int32, may be NULL).
+ *            No kernel traps. Every bounded wait inside a kernel gives up after about one
+ *            second and sets PA_ERR_TIMEOUT.
+ *
+ * KV pool layout (one pool per layer, one for K and one for V):
+ *     pool[num_blocks][num_kv_heads][block_size][head_dim]   elements of kv_dtype
+ * so the keys of one (physical block, kv head) pair are one contiguous run of
+ * block_size * head_dim * elt bytes. Logical position t of a sequence lives in logical
+ * block t / block_size at slot t % block_size (0-indexed), i.e. physical block
+ * block_tables[seq][t / block_size].
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* pa_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  PA_OK = 0,
+  PA_EINVAL = 1,        /* invalid argument; nothing was enqueued */
+  PA_EUNSUPPORTED = 2,  /* valid but not built: dtype / head_dim / group combination */
+  PA_ECUDA = 3          /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum {
+  PA_F16 = 0,       /* IEEE binary16 */
+  PA_BF16 = 1,      /* bfloat16 */
+  PA_FP8_E4M3 = 2   /* OCP FP8 E4M3 (raw bytes), dequantised with a per-tensor fp32 scale */
+} pa_dtype;
+
+typedef enum {
+  PA_SWAP_OUT = 0,  /* device pool blocks -> pinned host buffer */
+  PA_SWAP_IN = 1    /* pinned host buffer -> device pool blocks */
+} pa_swap_dir;
+
+/* Bits OR-ed into the optional device error flag. */
+#define PA_ERR_BLOCK_ID 1 /* block table entry, slot or pair outside [0, num_blocks) */
+#define PA_ERR_CTX_LEN 2  /* ctx_len < 0, > max_ctx_len or > max_blocks_per_seq*block_size */
+#define PA_ERR_TIMEOUT 4  /* a bounded wait inside a kernel expired */
+
+/*
+ * pa_decode - single-token decode attention over a paged KV pool.
+ *
+ * Source: PagedAttention summary page, paragraph on the PagedAttention kernel (block K_j holds
+ * the keys of tokens (j-1)B+1..jB, the kernel fetches each block wherever it is stored and the
+ * result is identical to ordinary attention) and paragraph on the block table (logical blocks
+ * filled left to right, a filled-slot count per sequence).
+ *
+ * For sequence s with L = ctx_lens[s] and query head h (group g = h / (num_q_heads/num_kv_heads)):
+ *     K^[t] = k_pool[block_tables[s][t / B]][g][t % B][:] * k_scale      (t < L)
+ *     V^[t] = v_pool[...same...] * v_scale
+ *     s_t   = scale * <q[s][h], K^[t]>
+ *     out[s][h] = sum_t softmax(s)_t * V^[t]
+ * L includes the token written by pa_write_kv in the same step. L == 0 gives a zero row.
+ * Slots at positions >= L and block-table entries beyond ceil(L/B) are never read, so freed
+ * or unwritten slots may hold any bytes (including NaN patterns).
+ *
+ * Layouts (all device, contiguous, row-major):
+ *   q            [num_seqs][num_q_heads][head_dim]          q_dtype (PA_F16 or PA_BF16)
+ *   k_pool/v_pool [num_blocks][num_kv_heads][block_size][head_dim]   kv_dtype, 16-byte aligned
+ *   block_tables [num_seqs][max_blocks_per_seq]              int32 physical block ids
+ *   ctx_lens     [num_seqs]                                  int32
+ *   out          [num_seqs][num_q_heads][head_dim]           q_dtype
+ *   workspace    >= pa_decode_workspace_size(args) bytes, 256-byte aligned, contents ignored
+ * Supported: head_dim in {64, 128}; block_size in {4, 8, 16, 32}; group size
+ * num_q_heads/num_kv_heads in {1, 2, 4, 8, 16}; (q, kv) dtype pairs (F16, F16), (BF16, BF16),
+ * (F16, FP8_E4M3), (BF16, FP8_E4M3). k_scale / v_scale multiply the stored values (use 1.0
+ * for 16-bit KV). Work is split along the context ("split-K") when that improves occupancy;
+ * split_tokens = 0 lets the library choose, otherwise it must be a multiple of max(16, B).
+ */
+typedef struct pa_decode_args {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* ctx_lens;
+  void* out;
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t max_ctx_len;   /* host-known upper bound of ctx_lens; plans the split-K grid */
+  int32_t split_tokens;  /* 0 = automatic */
+  pa_dtype q_dtype;
+  pa_dtype kv_dtype;
+  float scale;           /* softmax scale, usually 1/sqrt(head_dim) */
+  float k_scale;         /* per-tensor dequantisation scale of K (1.0 for 16-bit KV) */
+  float v_scale;         /* per-tensor dequantisation scale of V (1.0 for 16-bit KV) */
+  void* workspace;       /* device scratch for split-K partials; may be NULL if size is 0 */
+  size_t workspace_bytes;
+  int32_t* err_flag;     /* device int32 or NULL */
+} pa_decode_args;
+
+/* Bytes of device workspace pa_decode needs for these arguments (0 when no split is used).
+ * Depends only on the sizes in args and on the current device's SM count. Returns 0 and sets
+ * the last-error message if the arguments are invalid. */
+size_t pa_decode_workspace_size(const pa_decode_args* args);
+
+/* Enqueue the decode described by args on stream. */
+pa_status pa_decode(const pa_decode_args* args, pa_stream stream);
+
+/*
+ * pa_write_kv - store each new token's key and value in its slot.
+ *
+ * Source: "When KV Capacity Runs Out", section "Pause requests and release KV blocks"
+ * (Figure 2: the KV of position 8 is written into the first slot of the block just linked
+ * into A's block table) and section "Running out of KV space during generation" (each processed
+ * input adds KV). For every token t with sigma = slot_mapping[t] >= 0 and every kv head h:
+ *     k_pool[sigma / block_size][h][sigma % block_size][:] = k[t][h][:]     (same for v)
+ * as a raw element copy in kv_dtype (fp8 bytes are copied, not re-quantised). sigma < 0 marks
+ * a padding token and is skipped; sigma >= num_blocks*block_size sets PA_ERR_BLOCK_ID.
+ * Two tokens with the same slot leave either token's data.
+ *   k, v          device [num_tokens][num_kv_heads][head_dim], kv_dtype, 16-byte aligned
+ *   k_pool,v_pool device pool layout above
+ *   slot_mapping  device int64 [num_tokens]
+ */
+pa_status pa_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
+                      const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t num_blocks, pa_dtype kv_dtype,
+                      int32_t* err_flag, pa_stream stream);
+
+/*
+ * pa_copy_blocks - copy-on-write duplication of whole physical blocks.
+ *
+ * Source: PagedAttention summary page, paragraph on sharing (a sample that must write into a
+ * shared block receives its own copy, as when a process forks) and paragraph on shared
+ * prefixes (the last prefix block is copy-on-write). For every pair p, every layer l and both
+ * pools:  pool_l[pairs[p][1]] = pool_l[pairs[p][0]]  (block_bytes bytes; source unchanged).
+ * All pairs form one parallel step: no destination may equal a source or another destination
+ * of the same call (results are unspecified otherwise).
+ *   k_pools, v_pools  HOST arrays of num_layers device pointers (one pool per layer),
+ *                     each 16-byte aligned; num_layers <= 256
+ *   pairs             device int32 [num_pairs][2] = (src, dst) physical block ids
+ *   block_bytes       num_kv_heads * block_size * head_dim * elt; a multiple of 16
+ * Ids outside [0, num_blocks) set PA_ERR_BLOCK_ID and that pair is skipped.
+ */
+pa_status pa_copy_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                         const int32_t* pairs, int32_t num_pairs, int32_t num_blocks,
+                         size_t block_bytes, int32_t* err_flag, pa_stream stream);
+
+/*
+ * pa_swap_blocks - move a preempted sequence's whole block set to pinned host memory and back.
+ *
+ * Source: "When KV Capacity Runs Out", section "Restore KV stored outside the GPU" (Figure 4:
+ * the KV is copied to CPU memory, the GPU blocks are released only after the copy finished,
+ * and it is later restored into blocks that may sit elsewhere); PagedAttention summary page,
+ * paragraph on all-or-nothing eviction; "KV Cache Preemption in vLLM", section "Swap versus
+ * recompute" (pinned memory; a block's data is spread over every layer).
+ *   PA_SWAP_OUT:  host_buf[i][l][0][:] = k_pools[l][block_ids[i]][...]
+ *                 host_buf[i][l][1][:] = v_pools[l][block_ids[i]][...]
+ *   PA_SWAP_IN:   the reverse assignment.
+ *   host_buf   pinned host, [n][num_layers][2][block_bytes] bytes, 16-byte aligned
+ *   block_ids  HOST int32 [n], each in [0, num_blocks) (checked on the host), no duplicates
+ *              for PA_SWAP_IN
+ *   staging    optional device buffer of >= n*num_layers*2*block_bytes bytes. NULL: the kernel
+ *              reads/writes the pinned buffer directly through its mapped device address.
+ *              Non-NULL: a gather/scatter kernel packs blocks into staging and one bulk
+ *              cudaMemcpyAsync crosses the host link.
+ * The caller must not reuse the blocks (swap-out) or the host buffer (swap-in) until the
+ * stream has passed this call.
+ */
+pa_status pa_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                         void* host_buf, const int32_t* block_ids, int32_t n, int32_t num_blocks,
+                         size_t block_bytes, pa_swap_dir dir, void* staging, size_t staging_bytes,
+                         pa_stream stream);
+
+/* Static description of a status code. */
+const char* pa_status_string(pa_status status);
+
+/* Detail for the latest non-OK status returned on the calling thread ("" if none). */
+const char* pa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */
