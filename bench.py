@@ -1,0 +1,625 @@
+"""Benchmark of the paged KV-cache hot path on one GB300 (or N replicas under torchrun).
+
+One step = one decode step of the shared-prompt GQA workload ("gqa_pressure": 100 sequences,
+32 query / 8 KV heads x 128, bf16, 16-token blocks, contexts U[256, 4096] raised to >= 513,
+25 groups of 4 sharing a 512-token prompt): pa_write_kv of the 100 new tokens, pa_copy_blocks of
+the 25 copy-on-write blocks, pa_decode (main kernel + split-K reduce), one layer. Inputs are
+resident in HBM and larger than L2; L2 is also flushed between timed steps (outside the events).
+
+The metric is achieved HBM bandwidth: algorithmic bytes of the step (every distinct KV byte the
+attention must read once, the query/output, block tables, split partials written and read back,
+and the bytes the movers read and write) divided by the step time, plus decode tokens/s
+(sequences per second for this one layer). Run ``python bench.py --help`` for options.
+
+``--impl reference`` times the CPU oracle (the only other implementation; there is no runnable
+reference code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "gqa_pressure"
+SEED = 38 + 2  # seed = 38 + index of the configuration
+METRIC = "paged-decode attention: achieved HBM GB/s & % of peak; decode tokens/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
+DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh", "pa_decode_host.cu", "pa_decode_bf16.cu"]
+
+
+def split_tokens_for(spec: synth.DecodeSpec) -> int:
+    """Context split used by the benchmark (and by the full-size parity tests): ~256 KiB of K+V."""
+    elt = synth.ELT_BYTES[spec.kv_dtype]
+    return (256 * 1024) // (2 * spec.head_dim * elt)
+
+
+# ---------------------------------------------------------------------------- byte accounting
+
+def unique_kv_bytes(case: synth.PagedCase) -> int:
+    """Distinct K+V bytes the attention must read: every referenced physical block counted once,
+    with as many slots as the longest sequence that reads it has filled."""
+    spec = case.spec
+    B = spec.block_size
+    tables = case.block_tables.cpu().numpy()
+    lens = case.ctx_lens.cpu().numpy()
+    filled = {}
+    for s, L in enumerate(lens):
+        nb = (int(L) + B - 1) // B
+        for j in range(nb):
+            n = min(B, int(L) - j * B)
+            b = int(tables[s, j])
+            filled[b] = max(filled.get(b, 0), n)
+    row = spec.num_kv_heads * spec.head_dim * synth.ELT_BYTES[spec.kv_dtype]
+    return 2 * row * sum(filled.values())
+
+
+def logical_kv_bytes(case: synth.PagedCase) -> int:
+    spec = case.spec
+    row = spec.num_kv_heads * spec.head_dim * synth.ELT_BYTES[spec.kv_dtype]
+    return 2 * row * int(case.ctx_lens.sum())
+
+
+def decode_bytes(case: synth.PagedCase, split_tokens: int) -> dict:
+    spec = case.spec
+    lens = case.ctx_lens.cpu().numpy().astype(np.int64)
+    B = spec.block_size
+    qo = 2 * spec.num_seqs * spec.num_q_heads * spec.head_dim * 2
+    tables = 4 * int(((lens + B - 1) // B).sum()) + 4 * spec.num_seqs
+    nsplit = (lens + split_tokens - 1) // split_tokens
+    multi = nsplit[nsplit > 1]
+    partials = 2 * int(multi.sum()) * spec.num_q_heads * (spec.head_dim * 4 + 8)
+    kv = unique_kv_bytes(case)
+    return {"kv_unique": kv, "kv_logical": logical_kv_bytes(case), "q_out": qo,
+            "tables": tables, "partials": partials, "total": kv + qo + tables + partials}
+
+
+def mover_bytes(case: synth.PagedCase) -> dict:
+    spec = case.spec
+    row = spec.num_kv_heads * spec.head_dim * synth.ELT_BYTES[spec.kv_dtype]
+    write = 2 * 2 * spec.num_seqs * row + 8 * spec.num_seqs      # read new K,V + write slots
+    copy = 2 * 2 * case.cow_pairs.shape[0] * case.block_bytes + 8 * case.cow_pairs.shape[0]
+    return {"write_kv": write, "copy_blocks": copy}
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_38_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    want = decode_source_hash()
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == "pa_decode_kernel" \
+                    and parts[1] == workload and parts[2] == want:
+                return int(parts[3])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------- our arm
+
+class Step:
+    """One decode step of the workload through the library's binding."""
+
+    def __init__(self, case: synth.PagedCase, split_tokens: int):
+        import paged_kv_cache_38_gb300 as pa
+
+        self.pa = pa
+        self.case = case
+        self.split = split_tokens
+        self.max_ctx = int(case.ctx_lens.max())
+        self.out = torch.empty_like(case.q)
+        args = pa.make_decode_args(case.q, case.k_pool, case.v_pool, case.block_tables,
+                                   case.ctx_lens, self.out, scale=case.scale,
+                                   max_ctx_len=self.max_ctx, split_tokens=split_tokens)
+        need = pa.pa_decode_workspace_size(args)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=case.q.device)
+        self.max_splits = (self.max_ctx + split_tokens - 1) // split_tokens
+        self.launches = 3 + (1 if self.max_splits > 1 else 0)
+
+    def decode(self, q=None, block_tables=None, ctx_lens=None, out=None):
+        c = self.case
+        return self.pa.pa_decode(c.q if q is None else q, c.k_pool, c.v_pool,
+                                 c.block_tables if block_tables is None else block_tables,
+                                 c.ctx_lens if ctx_lens is None else ctx_lens, c.scale,
+                                 out=self.out if out is None else out, k_scale=c.k_scale,
+                                 v_scale=c.v_scale, max_ctx_len=self.max_ctx,
+                                 split_tokens=self.split, workspace=self.ws)
+
+    def run(self):
+        c = self.case
+        self.pa.pa_write_kv(c.k_new, c.v_new, c.k_pool, c.v_pool, c.slot_mapping)
+        if c.cow_pairs.numel():
+            self.pa.pa_copy_blocks([c.k_pool], [c.v_pool], c.cow_pairs)
+        return self.decode()
+
+
+def time_steps(fn, steps: int, flush: torch.Tensor):
+    """Per-step CUDA-event times (ms) on the current stream, L2 flushed before each step."""
+    times = []
+    stream = torch.cuda.current_stream()
+    for _ in range(steps):
+        flush.fill_(1)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def run_ours(args, world, rank, local) -> None:
+    import paged_kv_cache_38_gb300 as pa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pa.lib()
+    spec = synth.SPECS[args.workload]
+    case = synth.make_case(spec, seed=SEED, device=dev, logical=False, poison=False)
+    split = args.split_tokens or split_tokens_for(spec)
+    step = Step(case, split)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    dbytes = decode_bytes(case, split)
+    mbytes = mover_bytes(case)
+    step_bytes = dbytes["total"] + mbytes["write_kv"] + mbytes["copy_blocks"]
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        times = time_steps(step.run, args.steps, flush)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    total_ms = max_over_ranks(sum(times), world)
+    ms_per_step = total_ms / args.steps
+
+    # ---- the decode call alone (main kernel + split-K reduce), same stream, L2 flushed
+    dtimes = time_steps(step.decode, max(args.steps, 10), flush)
+    dec_ms = statistics.mean(dtimes)
+
+    # ---- end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(step, case, args.steps, flush, step_bytes)
+
+    peaks = load_peaks()
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    dec_gbs = dbytes["total"] / (dec_ms * 1e-3) / 1e9
+    extra = {}
+    if rank == 0 and not args.quick:
+        extra = run_extras(args, dev, flush, peaks)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, split, args.cpu_seconds)
+
+    if rank != 0:
+        return
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded block pools shaped like the pages' workloads)",
+        "config": {
+            "workload": (f"{args.workload}: {spec.num_seqs} seqs, {spec.num_q_heads} q / "
+                         f"{spec.num_kv_heads} kv heads x {spec.head_dim}, {spec.kv_dtype} KV, "
+                         f"block {spec.block_size}, ctx U{list(spec.ctx_range)} (>= "
+                         f"{spec.shared_prompt + 1}), {spec.num_seqs // spec.group_size} groups x "
+                         f"{spec.group_size} share a {spec.shared_prompt}-token prompt, "
+                         f"{case.cow_pairs.shape[0]} CoW copies/step, 1 layer"),
+            "step": "pa_write_kv + pa_copy_blocks + pa_decode (main + split-K reduce)",
+            "split_tokens": split, "num_blocks": case.num_blocks,
+            "ctx_tokens": int(case.ctx_lens.sum()), "l2": "flushed between steps (untimed); "
+            "pool larger than L2", "parallelism": f"replicas x{world}",
+        },
+        "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 1),
+        "decode_tokens_per_s": round(world * spec.num_seqs / (ms_per_step * 1e-3), 1),
+        "bytes_per_step": {**dbytes, **mbytes, "total": step_bytes},
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (main + split-K reduce)",
+                     "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
+                     "peak_source": peaks["source"], "unit": "GB/s",
+                     "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "algorithmic_bytes": dbytes["total"], "ms_per_launch": round(dec_ms, 4)},
+        "gpu_launches": step.launches * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if extra:
+        line["extra"] = extra
+    print(json.dumps(line))
+
+
+def run_e2e(step: Step, case: synth.PagedCase, steps: int, flush, step_bytes: int) -> dict:
+    """Same step with inputs copied from pinned host memory and the output read back."""
+    host = {k: getattr(case, k).cpu().pin_memory()
+            for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "ctx_lens",
+                      "cow_pairs")}
+    dev = {k: torch.empty_like(v, device=case.q.device) for k, v in host.items()}
+    out_host = torch.empty(case.q.shape, dtype=case.q.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    pa = step.pa
+    c = case
+
+    def one():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        pa.pa_write_kv(dev["k_new"], dev["v_new"], c.k_pool, c.v_pool, dev["slot_mapping"])
+        pa.pa_copy_blocks([c.k_pool], [c.v_pool], dev["cow_pairs"])
+        out = step.decode(q=dev["q"], block_tables=dev["block_tables"], ctx_lens=dev["ctx_lens"])
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    times = time_steps(one, steps, flush)
+    ms = statistics.mean(times)
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------- other workloads
+
+def run_extras(args, dev, flush, peaks) -> dict:
+    """The other configurations of the pages: MHA fp16, FP8 long contexts, the preemption swap
+    and a large copy-on-write batch. Each is timed like the main step; all report GB/s."""
+    import paged_kv_cache_38_gb300 as pa
+
+    res = {}
+    for name in ("mha7b", "fp8_long"):
+        spec = synth.SPECS[name]
+        case = synth.make_case(spec, seed=SEED - 2 + (1 if name == "mha7b" else 3), device=dev,
+                               logical=False, poison=False)
+        split = split_tokens_for(spec)
+        st = Step(case, split)
+        for _ in range(3):
+            st.decode()
+        t = statistics.mean(time_steps(st.decode, 10, flush))
+        b = decode_bytes(case, split)
+        res[name] = {"decode_ms": round(t, 4), "gbs": round(b["total"] / (t * 1e-3) / 1e9, 1),
+                     "pct_of_peak": round(100 * b["total"] / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 1),
+                     "tokens_per_s": round(spec.num_seqs / (t * 1e-3), 1),
+                     "split_tokens": split, "bytes": b["total"]}
+        del case, st
+        torch.cuda.empty_cache()
+    res["preemption_swap"] = run_swap_bench(dev)
+    res["copy_blocks_large"] = run_copy_bench(dev, flush, peaks)
+    return res
+
+
+def run_swap_bench(dev) -> dict:
+    import paged_kv_cache_38_gb300 as pa
+
+    spec = synth.SPECS["preemption"]
+    case = synth.make_case(spec, seed=SEED + 3, device=dev, logical=False, poison=False)
+    victim = spec.num_seqs - 1
+    out_ids, in_ids = synth.swap_plan(case, victim, seed=SEED)
+    n, L, bb = len(out_ids), spec.num_layers, case.block_bytes
+    total = n * L * 2 * bb
+    host = torch.empty(total, dtype=torch.uint8).pin_memory()
+    staging = torch.empty(total, dtype=torch.uint8, device=dev)
+    res = {"blocks": n, "bytes_each_way": total}
+
+    def timed(fn, reps=5):
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return min(ts), statistics.mean(ts)
+
+    # host link peak: one large pinned copy each way
+    big = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    big_h = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    d2h_ms, _ = timed(lambda: big_h.copy_(big, non_blocking=True))
+    h2d_ms, _ = timed(lambda: big.copy_(big_h, non_blocking=True))
+    res["link_peak_d2h_gbs"] = round((1 << 30) / (d2h_ms * 1e-3) / 1e9, 1)
+    res["link_peak_h2d_gbs"] = round((1 << 30) / (h2d_ms * 1e-3) / 1e9, 1)
+    del big, big_h
+    ref = None
+    for mode, stg in (("direct", None), ("staged", staging)):
+        o_ms, _ = timed(lambda: pa.pa_swap_blocks(case.k_pools, case.v_pools, host, out_ids,
+                                                  pa.PA_SWAP_OUT, staging=stg))
+        i_ms, _ = timed(lambda: pa.pa_swap_blocks(case.k_pools, case.v_pools, host, in_ids,
+                                                  pa.PA_SWAP_IN, staging=stg))
+        res[f"{mode}_out_ms"] = round(o_ms, 3)
+        res[f"{mode}_in_ms"] = round(i_ms, 3)
+        res[f"{mode}_out_gbs"] = round(total / (o_ms * 1e-3) / 1e9, 1)
+        res[f"{mode}_in_gbs"] = round(total / (i_ms * 1e-3) / 1e9, 1)
+    # bit-exact round trip and an identical resumed decode
+    bt = case.block_tables.clone()
+    split = split_tokens_for(spec)
+    st = Step(case, split)
+    before = st.decode().clone()
+    pa.pa_swap_blocks(case.k_pools, case.v_pools, host, out_ids, pa.PA_SWAP_OUT)
+    for p in case.k_pools + case.v_pools:
+        p.view(torch.uint8).view(case.num_blocks, -1)[torch.from_numpy(out_ids).long().to(dev)] = 0
+    pa.pa_swap_blocks(case.k_pools, case.v_pools, host, in_ids, pa.PA_SWAP_IN)
+    bt[victim, :n] = torch.from_numpy(in_ids).to(dev)
+    after = st.decode(block_tables=bt).clone()
+    res["round_trip_decode_bit_exact"] = bool(torch.equal(before[victim], after[victim]))
+    res["vs_pages_context"] = "pages: ~3 ms each way for 188 MiB over PCIe Gen5 x16 (estimate)"
+    del case, st, staging, host
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_copy_bench(dev, flush, peaks) -> dict:
+    """pa_copy_blocks at the preemption geometry: 4,096 disjoint pairs x 32 layers, plus the
+    25-pair step of the GQA workload as a latency figure."""
+    import paged_kv_cache_38_gb300 as pa
+
+    layers, nblk, bb = 32, 8192 + 64, 32 * 1024
+    k = [torch.empty(nblk, bb, dtype=torch.uint8, device=dev) for _ in range(layers)]
+    v = [torch.empty(nblk, bb, dtype=torch.uint8, device=dev) for _ in range(layers)]
+    perm = torch.from_numpy(np.random.default_rng(SEED).permutation(nblk)[:8192].astype(np.int32))
+    pairs = torch.stack([perm[:4096], perm[4096:]], 1).contiguous().to(dev)
+    moved = 2 * 2 * 4096 * layers * bb
+    pa.pa_copy_blocks(k, v, pairs)
+    t = statistics.mean(time_steps(lambda: pa.pa_copy_blocks(k, v, pairs), 5, flush))
+    small = pairs[:25].contiguous()
+    ts = statistics.mean(time_steps(lambda: pa.pa_copy_blocks(k[:1], v[:1], small), 20, flush))
+    gbs = moved / (t * 1e-3) / 1e9
+    res = {"pairs": 4096, "layers": layers, "bytes_moved": moved, "ms": round(t, 3),
+           "gbs": round(gbs, 1), "pct_of_peak": round(100 * gbs / peaks["hbm_gbs"], 1),
+           "cow_25_pairs_us": round(ts * 1e3, 2)}
+    del k, v
+    torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(case: synth.PagedCase, split: int, seconds: float) -> dict:
+    """The fp64 oracle as it stands, on all host cores, over a seeded sample of the step's
+    sequences (whole step: write, copy, decode), scaled to the same GB/s metric."""
+    import oracle
+
+    orc = oracle.load()
+    spec = case.spec
+    kp = case.k_pool.cpu().view(torch.uint8).numpy().reshape(-1).copy()
+    vp = case.v_pool.cpu().view(torch.uint8).numpy().reshape(-1).copy()
+    q = case.q.cpu()
+    bt, cl = case.block_tables.cpu(), case.ctx_lens.cpu()
+    rng = np.random.default_rng(SEED)
+    order = rng.permutation(spec.num_seqs)
+    done, t0, byts = 0, time.perf_counter(), 0
+    row = spec.num_kv_heads * spec.head_dim * synth.ELT_BYTES[spec.kv_dtype]
+    orc.write_kv(case.k_new.cpu(), case.v_new.cpu(), kp, vp, case.slot_mapping.cpu(),
+                 num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                 block_size=spec.block_size, kv_dtype=spec.kv_dtype)
+    while done < spec.num_seqs and time.perf_counter() - t0 < seconds:
+        idx = torch.as_tensor(order[done:done + 4], dtype=torch.long)
+        orc.decode(q[idx], kp, vp, bt[idx], cl[idx], q_dtype=spec.q_dtype,
+                   kv_dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
+                   num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                   block_size=spec.block_size, scale=case.scale)
+        byts += 2 * row * int(cl[idx].sum()) + 2 * len(idx) * spec.num_q_heads * spec.head_dim * 2
+        done += len(idx)
+    el = time.perf_counter() - t0
+    return {"value": round(byts / el / 1e9, 3), "unit": "GB/s", "cores": orc.max_threads(),
+            "kind": "oracle", "seconds": round(el, 2),
+            "sample": f"write_kv of the step + oracle decode of {done} of {spec.num_seqs} "
+                      f"sequences (seeded order), logical KV bytes per second"}
+
+
+def run_reference(args, world, rank) -> None:
+    """Reference arm: the CPU oracle timed on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    spec = synth.SPECS[args.workload]
+    case = synth.make_case(spec, seed=SEED, device="cpu", logical=False, poison=False)
+    orc = oracle.load()
+    kp = case.k_pool.view(torch.uint8).numpy().reshape(-1).copy()
+    vp = case.v_pool.view(torch.uint8).numpy().reshape(-1).copy()
+    rng = np.random.default_rng(SEED)
+    sample = 8
+    row = spec.num_kv_heads * spec.head_dim * synth.ELT_BYTES[spec.kv_dtype]
+
+    def one(seqs):
+        idx = torch.as_tensor(seqs, dtype=torch.long)
+        orc.write_kv(case.k_new[idx], case.v_new[idx], kp, vp, case.slot_mapping[idx],
+                     num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                     block_size=spec.block_size, kv_dtype=spec.kv_dtype)
+        orc.decode(case.q[idx], kp, vp, case.block_tables[idx], case.ctx_lens[idx],
+                   q_dtype=spec.q_dtype, kv_dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
+                   num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                   block_size=spec.block_size, scale=case.scale)
+        return 2 * row * int(case.ctx_lens[idx].sum()) + 4 * len(seqs) * row
+
+    for _ in range(args.warmup):
+        one(rng.choice(spec.num_seqs, sample, replace=False))
+    t0 = time.perf_counter()
+    byts = 0
+    for _ in range(args.steps):
+        byts += one(rng.choice(spec.num_seqs, sample, replace=False))
+    el = time.perf_counter() - t0
+    value = byts / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload} (sample of {sample} sequences per step)"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{sample} seeded sequences per step: write_kv + decode"},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.SPECS))
+    ap.add_argument("--split-tokens", type=int, default=0)
+    ap.add_argument("--quick", action="store_true", help="skip the other configurations")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

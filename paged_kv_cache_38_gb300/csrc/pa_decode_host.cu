@@ -1,0 +1,291 @@
+// pa_decode_host.cu - validation, launch planning and tensor maps for pa_decode.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "pa_decode.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+int log2i(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// The pool as a 2-D tensor [num_blocks*num_kv_heads*block_size rows][head_dim] with a box of
+// one (block, kv head) tile: block_size rows x 128 bytes, 128-byte swizzle.
+pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_decode_args& a, int elt,
+                          std::string& msg) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) {
+    msg = "cuTensorMapEncodeTiled is not available from the driver";
+    return PA_ECUDA;
+  }
+  const cuuint64_t rows = static_cast<cuuint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.head_dim), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.head_dim) * elt};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(a.block_size)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                   2, const_cast<void*>(pool), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    msg = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
+    return PA_ECUDA;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+
+pa_status cuda_status(cudaError_t e, const char* what, std::string& msg) {
+  if (e == cudaSuccess) return PA_OK;
+  msg = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return PA_ECUDA;
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+pa_status check_decode_args(const pa_decode_args& a, bool check_pointers, std::string& msg) {
+  if (a.num_seqs < 0 || a.num_q_heads <= 0 || a.num_kv_heads <= 0 || a.num_blocks <= 0 ||
+      a.max_blocks_per_seq <= 0 || a.max_ctx_len < 0) {
+    msg = "sizes must be positive (num_seqs and max_ctx_len may be 0)";
+    return PA_EINVAL;
+  }
+  if (a.num_q_heads % a.num_kv_heads != 0) {
+    msg = "num_q_heads must be a multiple of num_kv_heads";
+    return PA_EINVAL;
+  }
+  const int group = a.num_q_heads / a.num_kv_heads;
+  if (a.block_size != 4 && a.block_size != 8 && a.block_size != 16 && a.block_size != 32) {
+    msg = "block_size must be 4, 8, 16 or 32";
+    return PA_EINVAL;
+  }
+  if (a.head_dim != 64 && a.head_dim != 128) {
+    msg = "head_dim must be 64 or 128";
+    return PA_EINVAL;
+  }
+  if (a.q_dtype != PA_F16 && a.q_dtype != PA_BF16) {
+    msg = "q_dtype must be PA_F16 or PA_BF16";
+    return PA_EINVAL;
+  }
+  if (a.kv_dtype != PA_F16 && a.kv_dtype != PA_BF16 && a.kv_dtype != PA_FP8_E4M3) {
+    msg = "unknown kv_dtype";
+    return PA_EINVAL;
+  }
+  if (a.kv_dtype != PA_FP8_E4M3 && a.kv_dtype != a.q_dtype) {
+    msg = "for 16-bit KV the query dtype must equal the KV dtype";
+    return PA_EUNSUPPORTED;
+  }
+  if (a.kv_dtype == PA_FP8_E4M3 && a.head_dim != 128) {
+    msg = "E4M3 KV is built for head_dim 128";
+    return PA_EUNSUPPORTED;
+  }
+  if (!(group == 1 || group == 2 || group == 4 || group == 8 || group == 16)) {
+    msg = "num_q_heads / num_kv_heads must be 1, 2, 4, 8 or 16";
+    return PA_EUNSUPPORTED;
+  }
+  if (a.max_ctx_len > a.max_blocks_per_seq * a.block_size) {
+    msg = "max_ctx_len exceeds max_blocks_per_seq * block_size";
+    return PA_EINVAL;
+  }
+  const long long rows = static_cast<long long>(a.num_blocks) * a.num_kv_heads * a.block_size;
+  if (rows >= (1ll << 31)) {
+    msg = "pool has more than 2^31 token rows per kv head layout";
+    return PA_EUNSUPPORTED;
+  }
+  if (a.num_seqs > 65535) {
+    msg = "num_seqs must be <= 65535";
+    return PA_EUNSUPPORTED;
+  }
+  if (check_pointers && a.num_seqs > 0) {
+    if (!a.q || !a.k_pool || !a.v_pool || !a.block_tables || !a.ctx_lens || !a.out) {
+      msg = "null pointer argument";
+      return PA_EINVAL;
+    }
+    if (!aligned(a.q, 16) || !aligned(a.k_pool, 16) || !aligned(a.v_pool, 16) ||
+        !aligned(a.out, 4) || !aligned(a.block_tables, 4) || !aligned(a.ctx_lens, 4)) {
+      msg = "q, k_pool, v_pool must be 16-byte aligned; out, tables, ctx_lens 4-byte aligned";
+      return PA_EINVAL;
+    }
+  }
+  if (!(a.scale == a.scale) || !(a.k_scale == a.k_scale) || !(a.v_scale == a.v_scale)) {
+    msg = "scale, k_scale and v_scale must not be NaN";
+    return PA_EINVAL;
+  }
+  if (a.split_tokens < 0) {
+    msg = "split_tokens must be >= 0";
+    return PA_EINVAL;
+  }
+  return PA_OK;
+}
+
+pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std::string& msg) {
+  pa_status st = check_decode_args(a, false, msg);
+  if (st != PA_OK) return st;
+  const int B = a.block_size, D = a.head_dim;
+  const int group = a.num_q_heads / a.num_kv_heads;
+  pl.elt = a.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
+  pl.regions = D * pl.elt / 128;
+  pl.stage_tokens = std::max(16, B);
+  pl.region_stride = std::max(B * 128, 1024);
+  pl.stage_bytes = (pl.stage_tokens / B) * pl.regions * pl.region_stride;
+  int stages = 65536 / (2 * pl.stage_bytes);
+  stages = (stages / kConsumerWarps) * kConsumerWarps;
+  pl.stages = std::min(kMaxStages, std::max(kConsumerWarps, stages));
+
+  const int stok = pl.stage_tokens;
+  if (a.split_tokens > 0) {
+    if (a.split_tokens % stok != 0) {
+      msg = "split_tokens must be a multiple of max(16, block_size)";
+      return PA_EINVAL;
+    }
+    pl.split_tokens = a.split_tokens;
+  } else {
+    // about 256 KiB of K+V per split, fewer tokens when the grid would not fill the GPU
+    int tokens = (256 * 1024) / (2 * D * pl.elt);
+    const long long units = static_cast<long long>(a.num_seqs) * a.num_kv_heads;
+    const int sms = sm_count > 0 ? sm_count : 148;
+    while (tokens > 4 * stok && units * ((a.max_ctx_len + tokens - 1) / tokens) < 4LL * sms)
+      tokens /= 2;
+    pl.split_tokens = std::max(stok, (tokens / stok) * stok);
+  }
+  pl.max_splits = std::max(1, (a.max_ctx_len + pl.split_tokens - 1) / pl.split_tokens);
+  if (pl.max_splits > 65535) {
+    msg = "too many context splits; raise split_tokens";
+    return PA_EINVAL;
+  }
+  const int merge = kConsumerWarps * group * D * 4 + kConsumerWarps * group * 8;
+  pl.ctl_offset = ((std::max(pl.stages * 2 * pl.stage_bytes, merge) + 15) / 16) * 16;
+  const int table_entries = pl.split_tokens / B + 1;
+  pl.smem_bytes = 1024 + pl.ctl_offset + 2 * kMaxStages * 8 + 16 + table_entries * 4;
+  if (pl.smem_bytes > 227 * 1024) {
+    msg = "split_tokens too large for the shared-memory block-table slice";
+    return PA_EINVAL;
+  }
+  if (pl.max_splits > 1) {
+    const size_t slots = static_cast<size_t>(a.num_seqs) * a.num_q_heads * pl.max_splits;
+    pl.workspace = ((slots * D * 4 + 255) / 256) * 256 + slots * 8;
+  } else {
+    pl.workspace = 0;
+  }
+  return PA_OK;
+}
+
+pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& msg) {
+  DecodePlan pl;
+  pa_status st = check_decode_args(a, true, msg);
+  if (st != PA_OK) return st;
+  st = plan_decode(a, device_sm_count(), pl, msg);
+  if (st != PA_OK) return st;
+  if (pl.workspace > 0) {
+    if (a.workspace == nullptr || a.workspace_bytes < pl.workspace) {
+      msg = "workspace smaller than pa_decode_workspace_size()";
+      return PA_EINVAL;
+    }
+    if (!aligned(a.workspace, 256)) {
+      msg = "workspace must be 256-byte aligned";
+      return PA_EINVAL;
+    }
+  }
+  if (a.num_seqs == 0) return PA_OK;
+
+  CUtensorMap kmap, vmap;
+  st = encode_pool_map(&kmap, a.k_pool, a, pl.elt, msg);
+  if (st != PA_OK) return st;
+  st = encode_pool_map(&vmap, a.v_pool, a, pl.elt, msg);
+  if (st != PA_OK) return st;
+
+  DecodeParams p{};
+  p.q = a.q;
+  p.out = a.out;
+  p.block_tables = a.block_tables;
+  p.ctx_lens = a.ctx_lens;
+  const size_t slots = static_cast<size_t>(a.num_seqs) * a.num_q_heads * pl.max_splits;
+  p.part_o = pl.workspace ? static_cast<float*>(a.workspace) : nullptr;
+  p.part_ml = pl.workspace ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) +
+                                                       ((slots * a.head_dim * 4 + 255) / 256) * 256)
+                           : nullptr;
+  p.err = a.err_flag;
+  p.num_seqs = a.num_seqs;
+  p.num_q_heads = a.num_q_heads;
+  p.num_kv_heads = a.num_kv_heads;
+  p.block_size = a.block_size;
+  p.log2_block = log2i(a.block_size);
+  p.num_blocks = a.num_blocks;
+  p.max_blocks = a.max_blocks_per_seq;
+  p.max_ctx = a.max_ctx_len;
+  p.split_tokens = pl.split_tokens;
+  p.max_splits = pl.max_splits;
+  p.stages = pl.stages;
+  p.region_stride = pl.region_stride;
+  p.stage_bytes = pl.stage_bytes;
+  p.ctl_offset = pl.ctl_offset;
+  p.score_scale = a.scale * a.k_scale * kLog2e;
+  p.v_scale = a.v_scale;
+  p.q_bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
+
+  const int group = a.num_q_heads / a.num_kv_heads;
+  dim3 grid(pl.max_splits, a.num_kv_heads, a.num_seqs);
+  cudaError_t e;
+  switch (a.kv_dtype) {
+    case PA_F16:
+      e = launch_decode_f16(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
+      break;
+    case PA_BF16:
+      e = launch_decode_bf16(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
+      break;
+    default:
+      e = launch_decode_e4m3(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
+      break;
+  }
+  st = cuda_status(e, "pa_decode kernel launch", msg);
+  if (st != PA_OK) return st;
+  if (pl.max_splits > 1) {
+    e = launch_reduce(a.head_dim, p, a.q_dtype == PA_BF16, stream);
+    st = cuda_status(e, "pa_decode reduce launch", msg);
+  }
+  return st;
+}
+
+cudaError_t launch_reduce(int head_dim, const DecodeParams& p, bool out_bf16, cudaStream_t stream) {
+  const int warps = p.num_seqs * p.num_q_heads;
+  dim3 grid((warps + 3) / 4);
+  if (head_dim == 128)
+    pa_reduce_kernel<128><<<grid, 128, 0, stream>>>(p, out_bf16 ? 1 : 0);
+  else
+    pa_reduce_kernel<64><<<grid, 128, 0, stream>>>(p, out_bf16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,69 @@
+// pa_internal.h - host-side interfaces shared by the translation units of libpa.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+struct DecodeParams;
+
+// Sizes of one pa_decode launch, derived only from the arguments and the SM count.
+struct DecodePlan {
+  int elt = 2;            // bytes per KV element
+  int regions = 1;        // 128-byte column regions per token row
+  int stage_tokens = 16;  // tokens per pipeline stage (max(16, block_size))
+  int region_stride = 0;  // bytes of one region of one block inside a stage
+  int stage_bytes = 0;    // bytes of K (or V) per stage
+  int stages = 0;         // ring depth
+  int split_tokens = 0;   // tokens per context split
+  int max_splits = 1;
+  int ctl_offset = 0;     // start of barriers / table inside the aligned shared memory
+  size_t smem_bytes = 0;  // dynamic shared memory per CTA
+  size_t workspace = 0;   // bytes of split partials (0 when max_splits == 1)
+};
+
+// Validate decode arguments (no device access; pointers only when check_pointers). On failure
+// returns PA_EINVAL or PA_EUNSUPPORTED and fills msg.
+pa_status check_decode_args(const pa_decode_args& a, bool check_pointers, std::string& msg);
+pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& plan, std::string& msg);
+int device_sm_count();
+
+// Kernel launchers per KV dtype (one translation unit each).
+cudaError_t launch_decode_f16(int head_dim, int group, const CUtensorMap& kmap,
+                              const CUtensorMap& vmap, const DecodeParams& p, dim3 grid,
+                              size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_bf16(int head_dim, int group, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, const DecodeParams& p, dim3 grid,
+                               size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_e4m3(int head_dim, int group, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, const DecodeParams& p, dim3 grid,
+                               size_t smem, cudaStream_t stream);
+cudaError_t launch_reduce(int head_dim, const DecodeParams& p, bool out_bf16, cudaStream_t stream);
+
+pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& msg);
+
+// Block movers.
+pa_status run_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
+                       const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks, pa_dtype kv_dtype,
+                       int32_t* err_flag, cudaStream_t stream, std::string& msg);
+pa_status run_copy_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                          const int32_t* pairs, int32_t num_pairs, int32_t num_blocks,
+                          size_t block_bytes, int32_t* err_flag, cudaStream_t stream,
+                          std::string& msg);
+pa_status run_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                          void* host_buf, const int32_t* block_ids, int32_t n, int32_t num_blocks,
+                          size_t block_bytes, pa_swap_dir dir, void* staging, size_t staging_bytes,
+                          cudaStream_t stream, std::string& msg);
+
+// Sets msg from a CUDA error and returns PA_ECUDA (or PA_OK for cudaSuccess).
+pa_status cuda_status(cudaError_t e, const char* what, std::string& msg);
+
+}  // namespace pa

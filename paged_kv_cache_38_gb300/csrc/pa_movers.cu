@@ -1,0 +1,321 @@
+// pa_movers.cu - block data movers: write-KV scatter, copy-on-write block copy, swap out/in.
+//
+// Sources: "When KV Capacity Runs Out: Pausing and Resuming Requests", Figure 2 (the KV of a
+// newly processed position goes into its slot) and Figure 4 (a preempted request's KV is copied
+// to CPU memory and later restored, possibly into other blocks); "Efficient Memory Management
+// for Large Language Model Serving with PagedAttention" (summary page), paragraph on
+// copy-on-write; "KV Cache Preemption in vLLM", section "Swap versus recompute" (pinned memory,
+// a block's data is spread over every layer, so a swap moves 2 * layers slabs per block).
+//
+// All three are byte moves: 16-byte vector loads and stores, several in flight per thread.
+#include <algorithm>
+#include <cstring>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMaxLayers = 256;
+constexpr int kMaxIdsPerLaunch = 2048;
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;  // 16-byte vectors per thread per step
+constexpr int kSliceBytes = kCopyThreads * kCopyUnroll * 16;  // 16 KiB per CTA step
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ------------------------------------------------------------------ write-KV
+
+struct WriteParams {
+  const uint4* k;
+  const uint4* v;
+  uint4* k_pool;
+  uint4* v_pool;
+  const int64_t* slots;
+  int32_t* err;
+  int num_tokens, num_kv_heads, chunks_per_row, block_size, num_blocks;
+};
+
+// One thread per 16-byte chunk of one (token, kv head) row: pool[slot/B][h][slot%B][:] = new[t][h][:].
+__global__ void __launch_bounds__(256) pa_write_kv_kernel(const __grid_constant__ WriteParams p) {
+  const long long total =
+      static_cast<long long>(p.num_tokens) * p.num_kv_heads * p.chunks_per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % p.chunks_per_row);
+    const long long th = i / p.chunks_per_row;
+    const int h = static_cast<int>(th % p.num_kv_heads);
+    const int t = static_cast<int>(th / p.num_kv_heads);
+    const long long slot = __ldg(p.slots + t);
+    if (slot < 0) continue;  // padding token
+    const long long blk = slot / p.block_size;
+    if (blk >= p.num_blocks) {
+      if (h == 0 && c == 0) flag_error(p.err, kErrBlockId);
+      continue;
+    }
+    const long long src = th * p.chunks_per_row + c;
+    const long long dst =
+        ((blk * p.num_kv_heads + h) * p.block_size + slot % p.block_size) * p.chunks_per_row + c;
+    const uint4 kv = __ldg(p.k + src);
+    const uint4 vv = __ldg(p.v + src);
+    p.k_pool[dst] = kv;
+    p.v_pool[dst] = vv;
+  }
+}
+
+// ------------------------------------------------------------------ region copies
+
+enum CopyMode { kCopyPairs = 0, kPoolToBuf = 1, kBufToPool = 2 };
+
+struct CopyParams {
+  uint8_t* k[kMaxLayers];
+  uint8_t* v[kMaxLayers];
+  uint8_t* buf;          // host-mapped pinned buffer or device staging, [n][layers][2][bytes]
+  const int32_t* pairs;  // kCopyPairs: device [n][2]
+  int32_t* err;
+  int32_t ids[kMaxIdsPerLaunch];  // kPoolToBuf / kBufToPool: block ids of this launch
+  long long block_bytes;
+  int mode, n, num_layers, num_blocks, slices_per_region;
+};
+
+// Region r = ((i * layers) + l) * 2 + kv moves one (block, layer, K|V) slab of block_bytes.
+// Work unit = one 16 KiB slice of a region; each thread keeps 4 x 16 bytes in flight.
+__global__ void __launch_bounds__(kCopyThreads) pa_copy_regions_kernel(const __grid_constant__ CopyParams p) {
+  const long long regions = static_cast<long long>(p.n) * p.num_layers * 2;
+  const long long units = regions * p.slices_per_region;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const long long r = u / p.slices_per_region;
+    const int slice = static_cast<int>(u % p.slices_per_region);
+    const int kv = static_cast<int>(r & 1);
+    const int l = static_cast<int>((r >> 1) % p.num_layers);
+    const int i = static_cast<int>((r >> 1) / p.num_layers);
+    const uint8_t* src;
+    uint8_t* dst;
+    uint8_t* pool = kv ? p.v[l] : p.k[l];
+    if (p.mode == kCopyPairs) {
+      const int s = __ldg(p.pairs + 2 * i), d = __ldg(p.pairs + 2 * i + 1);
+      if (s < 0 || s >= p.num_blocks || d < 0 || d >= p.num_blocks) {
+        if (threadIdx.x == 0 && slice == 0 && l == 0 && kv == 0) flag_error(p.err, kErrBlockId);
+        continue;
+      }
+      src = pool + s * p.block_bytes;
+      dst = pool + d * p.block_bytes;
+    } else {
+      uint8_t* slab = pool + static_cast<long long>(p.ids[i]) * p.block_bytes;
+      uint8_t* packed = p.buf + r * p.block_bytes;
+      src = p.mode == kPoolToBuf ? slab : packed;
+      dst = p.mode == kPoolToBuf ? packed : slab;
+    }
+    const long long off0 = static_cast<long long>(slice) * kSliceBytes;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src + off0);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + off0);
+    const long long left = (p.block_bytes - off0) / 16;  // vectors remaining in this region
+    uint4 tmp[kCopyUnroll];
+#pragma unroll
+    for (int k = 0; k < kCopyUnroll; ++k) {
+      const long long idx = threadIdx.x + static_cast<long long>(k) * kCopyThreads;
+      if (idx < left) tmp[k] = s4[idx];
+    }
+#pragma unroll
+    for (int k = 0; k < kCopyUnroll; ++k) {
+      const long long idx = threadIdx.x + static_cast<long long>(k) * kCopyThreads;
+      if (idx < left) d4[idx] = tmp[k];
+    }
+  }
+}
+
+int copy_grid(long long units) {
+  const int sms = std::max(1, device_sm_count());
+  return static_cast<int>(std::max(1LL, std::min(units, static_cast<long long>(sms) * 16)));
+}
+
+pa_status check_pools(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                      size_t block_bytes, int32_t num_blocks, std::string& msg) {
+  if (num_layers <= 0 || num_layers > kMaxLayers) {
+    msg = "num_layers must be in [1, 256]";
+    return PA_EINVAL;
+  }
+  if (!k_pools || !v_pools) {
+    msg = "null pool array";
+    return PA_EINVAL;
+  }
+  if (block_bytes == 0 || block_bytes % 16 != 0) {
+    msg = "block_bytes must be a positive multiple of 16";
+    return PA_EINVAL;
+  }
+  if (num_blocks <= 0) {
+    msg = "num_blocks must be positive";
+    return PA_EINVAL;
+  }
+  for (int l = 0; l < num_layers; ++l) {
+    if (!k_pools[l] || !v_pools[l] || !aligned16(k_pools[l]) || !aligned16(v_pools[l])) {
+      msg = "pool pointer " + std::to_string(l) + " is null or not 16-byte aligned";
+      return PA_EINVAL;
+    }
+  }
+  return PA_OK;
+}
+
+void fill_pools(CopyParams& p, void* const* k_pools, void* const* v_pools, int32_t num_layers) {
+  for (int l = 0; l < num_layers; ++l) {
+    p.k[l] = static_cast<uint8_t*>(k_pools[l]);
+    p.v[l] = static_cast<uint8_t*>(v_pools[l]);
+  }
+}
+
+}  // namespace
+
+pa_status run_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
+                       const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks, pa_dtype kv_dtype,
+                       int32_t* err_flag, cudaStream_t stream, std::string& msg) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0) {
+    msg = "sizes must be positive (num_tokens may be 0)";
+    return PA_EINVAL;
+  }
+  if (kv_dtype != PA_F16 && kv_dtype != PA_BF16 && kv_dtype != PA_FP8_E4M3) {
+    msg = "unknown kv_dtype";
+    return PA_EINVAL;
+  }
+  const int elt = kv_dtype == PA_FP8_E4M3 ? 1 : 2;
+  if ((head_dim * elt) % 16 != 0) {
+    msg = "head_dim * element size must be a multiple of 16 bytes";
+    return PA_EINVAL;
+  }
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_pool || !v_pool || !slot_mapping) {
+    msg = "null pointer argument";
+    return PA_EINVAL;
+  }
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) {
+    msg = "k, v and the pools must be 16-byte aligned, slot_mapping 8-byte aligned";
+    return PA_EINVAL;
+  }
+  WriteParams p{};
+  p.k = static_cast<const uint4*>(k);
+  p.v = static_cast<const uint4*>(v);
+  p.k_pool = static_cast<uint4*>(k_pool);
+  p.v_pool = static_cast<uint4*>(v_pool);
+  p.slots = slot_mapping;
+  p.err = err_flag;
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = num_kv_heads;
+  p.chunks_per_row = head_dim * elt / 16;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  const long long total = static_cast<long long>(num_tokens) * num_kv_heads * p.chunks_per_row;
+  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256,
+                                                        std::max(1, device_sm_count()) * 8LL));
+  pa_write_kv_kernel<<<grid, 256, 0, stream>>>(p);
+  return cuda_status(cudaGetLastError(), "pa_write_kv launch", msg);
+}
+
+pa_status run_copy_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                          const int32_t* pairs, int32_t num_pairs, int32_t num_blocks,
+                          size_t block_bytes, int32_t* err_flag, cudaStream_t stream,
+                          std::string& msg) {
+  pa_status st = check_pools(k_pools, v_pools, num_layers, block_bytes, num_blocks, msg);
+  if (st != PA_OK) return st;
+  if (num_pairs < 0) {
+    msg = "num_pairs must be >= 0";
+    return PA_EINVAL;
+  }
+  if (num_pairs == 0) return PA_OK;
+  if (!pairs || (reinterpret_cast<uintptr_t>(pairs) & 3u)) {
+    msg = "pairs must be a 4-byte aligned device pointer";
+    return PA_EINVAL;
+  }
+  CopyParams* p = new CopyParams();
+  fill_pools(*p, k_pools, v_pools, num_layers);
+  p->pairs = pairs;
+  p->err = err_flag;
+  p->block_bytes = static_cast<long long>(block_bytes);
+  p->mode = kCopyPairs;
+  p->n = num_pairs;
+  p->num_layers = num_layers;
+  p->num_blocks = num_blocks;
+  p->slices_per_region = static_cast<int>((block_bytes + kSliceBytes - 1) / kSliceBytes);
+  const long long units = static_cast<long long>(num_pairs) * num_layers * 2 * p->slices_per_region;
+  pa_copy_regions_kernel<<<copy_grid(units), kCopyThreads, 0, stream>>>(*p);
+  delete p;
+  return cuda_status(cudaGetLastError(), "pa_copy_blocks launch", msg);
+}
+
+pa_status run_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                          void* host_buf, const int32_t* block_ids, int32_t n, int32_t num_blocks,
+                          size_t block_bytes, pa_swap_dir dir, void* staging, size_t staging_bytes,
+                          cudaStream_t stream, std::string& msg) {
+  pa_status st = check_pools(k_pools, v_pools, num_layers, block_bytes, num_blocks, msg);
+  if (st != PA_OK) return st;
+  if (dir != PA_SWAP_OUT && dir != PA_SWAP_IN) {
+    msg = "dir must be PA_SWAP_OUT or PA_SWAP_IN";
+    return PA_EINVAL;
+  }
+  if (n < 0) {
+    msg = "n must be >= 0";
+    return PA_EINVAL;
+  }
+  if (n == 0) return PA_OK;
+  if (!host_buf || !block_ids || !aligned16(host_buf)) {
+    msg = "host_buf (16-byte aligned) and block_ids are required";
+    return PA_EINVAL;
+  }
+  for (int i = 0; i < n; ++i) {
+    if (block_ids[i] < 0 || block_ids[i] >= num_blocks) {
+      msg = "block_ids[" + std::to_string(i) + "] is outside the pool";
+      return PA_EINVAL;
+    }
+  }
+  const size_t total = static_cast<size_t>(n) * num_layers * 2 * block_bytes;
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, host_buf) != cudaSuccess) {
+    cudaGetLastError();
+    msg = "host_buf is not known to CUDA";
+    return PA_EINVAL;
+  }
+  if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) {
+    msg = "host_buf must be pinned host memory (cudaHostAlloc / cudaHostRegister)";
+    return PA_EINVAL;
+  }
+  if (staging != nullptr && (staging_bytes < total || !aligned16(staging))) {
+    msg = "staging must hold n * num_layers * 2 * block_bytes bytes, 16-byte aligned";
+    return PA_EINVAL;
+  }
+  uint8_t* mapped = static_cast<uint8_t*>(attr.devicePointer);
+
+  if (staging != nullptr && dir == PA_SWAP_IN) {
+    st = cuda_status(cudaMemcpyAsync(staging, host_buf, total, cudaMemcpyHostToDevice, stream),
+                     "pa_swap_blocks host-to-device copy", msg);
+    if (st != PA_OK) return st;
+  }
+  CopyParams* p = new CopyParams();
+  fill_pools(*p, k_pools, v_pools, num_layers);
+  p->block_bytes = static_cast<long long>(block_bytes);
+  p->mode = dir == PA_SWAP_OUT ? kPoolToBuf : kBufToPool;
+  p->num_layers = num_layers;
+  p->num_blocks = num_blocks;
+  p->slices_per_region = static_cast<int>((block_bytes + kSliceBytes - 1) / kSliceBytes);
+  const size_t per_block = static_cast<size_t>(num_layers) * 2 * block_bytes;
+  uint8_t* buf = staging != nullptr ? static_cast<uint8_t*>(staging) : mapped;
+  for (int i0 = 0; i0 < n && st == PA_OK; i0 += kMaxIdsPerLaunch) {
+    const int cnt = std::min(kMaxIdsPerLaunch, n - i0);
+    std::memcpy(p->ids, block_ids + i0, sizeof(int32_t) * cnt);
+    p->n = cnt;
+    p->buf = buf + static_cast<size_t>(i0) * per_block;
+    const long long units = static_cast<long long>(cnt) * num_layers * 2 * p->slices_per_region;
+    pa_copy_regions_kernel<<<copy_grid(units), kCopyThreads, 0, stream>>>(*p);
+    st = cuda_status(cudaGetLastError(), "pa_swap_blocks launch", msg);
+  }
+  delete p;
+  if (st != PA_OK) return st;
+  if (staging != nullptr && dir == PA_SWAP_OUT) {
+    st = cuda_status(cudaMemcpyAsync(host_buf, staging, total, cudaMemcpyDeviceToHost, stream),
+                     "pa_swap_blocks device-to-host copy", msg);
+  }
+  return st;
+}
+
+}  // namespace pa

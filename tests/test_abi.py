@@ -1,0 +1,97 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every entry point the
+header declares, matches the binding's struct layout and validates arguments on the host."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_cache_38_gb300 as pa
+from paged_kv_cache_38_gb300 import build as pa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted([
+        "pa_copy_blocks", "pa_decode", "pa_decode_workspace_size", "pa_last_error_message",
+        "pa_status_string", "pa_swap_blocks", "pa_write_kv"])
+
+
+def test_library_exports_every_declared_symbol():
+    lib = pa.lib()
+    out = subprocess.run(["nm", "-D", "--defined-only", pa_build.LIBRARY], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s+(pa_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_struct_layout_matches_header(tmp_path):
+    fields = [f for f, _ in pa.pa.pa_decode_args._fields_]
+    src = tmp_path / "layout.c"
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "pa.h"', 'int main(void){',
+             'printf("%zu\\n", sizeof(pa_decode_args));']
+    lines += [f'printf("%zu\\n", offsetof(pa_decode_args, {f}));' for f in fields]
+    lines += ["return 0;}"]
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(pa.pa.pa_decode_args)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(pa.pa.pa_decode_args, f).offset == off, f
+
+
+def test_status_strings():
+    lib = pa.lib()
+    for code in (pa.PA_OK, pa.PA_EINVAL, pa.PA_EUNSUPPORTED, pa.PA_ECUDA):
+        assert lib.pa_status_string(code).startswith(b"PA_")
+
+
+def _args(**kw):
+    a = pa.pa.pa_decode_args()
+    base = dict(num_seqs=100, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                num_blocks=12000, max_blocks_per_seq=256, max_ctx_len=4096, q_dtype=pa.PA_BF16,
+                kv_dtype=pa.PA_BF16, scale=0.0884, k_scale=1.0, v_scale=1.0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_workspace_size_and_validation_on_host():
+    lib = pa.lib()
+    assert pa.pa_decode_workspace_size(_args()) > 0
+    assert pa.pa_decode_workspace_size(_args(max_ctx_len=16, split_tokens=16)) == 0
+    for bad in (dict(head_dim=96), dict(block_size=12), dict(num_q_heads=30),
+                dict(max_ctx_len=5000), dict(split_tokens=24)):
+        assert pa.pa_decode_workspace_size(_args(**bad)) == 0
+        assert lib.pa_last_error_message()
+    st = lib.pa_decode(ctypes.byref(_args(head_dim=96)), None)
+    assert st == pa.PA_EINVAL
+    st = lib.pa_decode(ctypes.byref(_args(num_q_heads=24)), None)  # group 3
+    assert st == pa.PA_EUNSUPPORTED
+    st = lib.pa_decode(ctypes.byref(_args()), None)  # null pointers
+    assert st == pa.PA_EINVAL
+    assert lib.pa_write_kv(None, None, None, None, None, 0, 8, 128, 16, 10, pa.PA_BF16, None,
+                           None) == pa.PA_OK
+    assert lib.pa_write_kv(None, None, None, None, None, 4, 8, 128, 16, 10, pa.PA_BF16, None,
+                           None) == pa.PA_EINVAL
+    arr = (ctypes.c_void_p * 1)(None)
+    assert lib.pa_copy_blocks(arr, arr, 0, None, 1, 10, 4096, None, None) == pa.PA_EINVAL
+    assert lib.pa_copy_blocks(arr, arr, 1, None, 1, 10, 4096, None, None) == pa.PA_EINVAL
+    ids = (ctypes.c_int32 * 1)(20)
+    assert lib.pa_swap_blocks(arr, arr, 1, None, ids, 1, 10, 4096, pa.PA_SWAP_OUT, None, 0,
+                              None) == pa.PA_EINVAL

@@ -1,0 +1,153 @@
+"""pa_write_kv, pa_copy_blocks and pa_swap_blocks on the GPU: bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import pins
+import synth
+from helpers import TOL, gpu_decode, max_abs_err, oracle_decode
+
+pytestmark = pytest.mark.gpu
+
+import paged_kv_cache_38_gb300 as pa  # noqa: E402
+
+
+def _u8(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.uint8).cpu().numpy().copy()
+
+
+@pytest.mark.parametrize("spec", pins.small_specs(), ids=[s.name for s in pins.small_specs()])
+def test_write_kv_bit_exact(spec):
+    case = synth.make_case(spec, seed=400)
+    orc = oracle.load()
+    # poison the slots being written, plus padding tokens (-1) and one repeated token
+    kp, vp = case.k_pool.clone(), case.v_pool.clone()
+    B = spec.block_size
+    raw_k = kp.view(torch.uint8).view(case.num_blocks, spec.num_kv_heads, B, -1)
+    raw_v = vp.view(torch.uint8).view(case.num_blocks, spec.num_kv_heads, B, -1)
+    for s in range(spec.num_seqs):
+        sig = int(case.slot_mapping[s])
+        if sig >= 0:
+            raw_k[sig // B, :, sig % B] = 0xFF
+            raw_v[sig // B, :, sig % B] = 0xFF
+    sm = torch.cat([case.slot_mapping, torch.tensor([-1, -7], dtype=torch.int64)])
+    knew = torch.cat([case.k_new, case.k_new[:2]])
+    vnew = torch.cat([case.v_new, case.v_new[:2]])
+    exp_k, exp_v = _u8(kp), _u8(vp)
+    assert orc.write_kv(knew, vnew, exp_k, exp_v, sm, num_kv_heads=spec.num_kv_heads,
+                        head_dim=spec.head_dim, block_size=B, kv_dtype=spec.kv_dtype) == 0
+    gk, gv = kp.cuda(), vp.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_write_kv(knew.cuda(), vnew.cuda(), gk, gv, sm.cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(_u8(gk), exp_k) and np.array_equal(_u8(gv), exp_v)
+
+
+def test_write_kv_out_of_pool_flagged():
+    spec = synth.SPECS["toy"]
+    case = synth.make_case(spec, seed=1).to("cuda")
+    before = case.k_pool.clone()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad = torch.tensor([case.num_blocks * spec.block_size + 3], dtype=torch.int64, device="cuda")
+    pa.pa_write_kv(case.k_new[:1], case.v_new[:1], case.k_pool, case.v_pool, bad, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_ERR_BLOCK_ID
+    assert torch.equal(before.view(torch.uint8), case.k_pool.view(torch.uint8))
+
+
+@pytest.mark.parametrize("layers,block_bytes_kib", [(1, 32), (3, 2), (4, 64)])
+def test_copy_blocks_bit_exact(layers, block_bytes_kib):
+    """Copy-on-write: destinations become source copies, sources and the rest stay unchanged."""
+    orc = oracle.load()
+    rng = np.random.default_rng(layers)
+    nblk = 64
+    bb = block_bytes_kib * 1024
+    kps = [rng.integers(0, 256, nblk * bb, dtype=np.uint8) for _ in range(layers)]
+    vps = [rng.integers(0, 256, nblk * bb, dtype=np.uint8) for _ in range(layers)]
+    perm = rng.permutation(nblk)
+    pairs = np.stack([perm[:20], perm[20:40]], axis=1).astype(np.int32)
+    gk = [torch.from_numpy(p.copy()).cuda().view(nblk, -1) for p in kps]
+    gv = [torch.from_numpy(p.copy()).cuda().view(nblk, -1) for p in vps]
+    assert orc.copy_blocks(kps, vps, pairs, block_bytes=bb) == 0
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks(gk, gv, torch.from_numpy(pairs).cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for l in range(layers):
+        assert np.array_equal(gk[l].cpu().numpy().reshape(-1), kps[l])
+        assert np.array_equal(gv[l].cpu().numpy().reshape(-1), vps[l])
+    bad = torch.tensor([[0, nblk]], dtype=torch.int32, device="cuda")
+    pa.pa_copy_blocks(gk, gv, bad, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_ERR_BLOCK_ID
+    assert np.array_equal(gk[0].cpu().numpy().reshape(-1), kps[0])
+
+
+def test_copy_blocks_cow_step_matches_decode():
+    """The per-group copy-on-write of the shared-prompt workload: poison the private copies,
+    copy, and the members that read them get the oracle's attention again."""
+    spec = synth.SPECS["gqa_pressure"].scaled(num_seqs=16, ctx_range=(100, 600), shared_prompt=64)
+    case = synth.make_case(spec, seed=41)
+    ref = oracle_decode(case)
+    g = case.to("cuda")
+    raw_k, raw_v = g.k_pool.view(torch.int16), g.v_pool.view(torch.int16)
+    dst = g.cow_pairs[:, 1].long()
+    raw_k[dst] = synth.NAN_BITS["bf16"]
+    raw_v[dst] = synth.NAN_BITS["bf16"]
+    pa.pa_copy_blocks([g.k_pool], [g.v_pool], g.cow_pairs)
+    assert max_abs_err(gpu_decode(g), ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("staged", [False, True])
+def test_swap_round_trip(staged):
+    """Swap a sequence's whole block set out to pinned memory and back into other blocks:
+    the host image matches the oracle's byte for byte and decode output is unchanged."""
+    spec = synth.SPECS["preemption"].scaled(num_seqs=12, ctx_range=(100, 900), shared_prompt=64,
+                                            num_layers=3, victim_len=400, occupancy=0.6)
+    case = synth.make_case(spec, seed=52, device="cuda", logical=False, poison=False)
+    victim = spec.num_seqs - 1
+    out_ids, in_ids = synth.swap_plan(case, victim, seed=3)
+    bb = case.block_bytes
+    n, L = len(out_ids), spec.num_layers
+    before = gpu_decode(case)
+    host = torch.zeros(n * L * 2 * bb, dtype=torch.uint8).pin_memory()
+    staging = torch.empty(n * L * 2 * bb, dtype=torch.uint8, device="cuda") if staged else None
+    pa.pa_swap_blocks(case.k_pools, case.v_pools, host, out_ids, pa.PA_SWAP_OUT, staging=staging)
+    torch.cuda.synchronize()
+    # oracle swap-out on host copies of the pools
+    kps = [_u8(p) for p in case.k_pools]
+    vps = [_u8(p) for p in case.v_pools]
+    exp = np.zeros(n * L * 2 * bb, np.uint8)
+    assert oracle.load().swap_blocks(kps, vps, exp, out_ids, block_bytes=bb, direction="out") == 0
+    assert np.array_equal(host.numpy(), exp)
+    # the released blocks are reused by someone else, then the victim comes back elsewhere
+    for p in case.k_pools + case.v_pools:
+        p.view(torch.uint8).view(case.num_blocks, -1)[torch.from_numpy(out_ids).long().cuda()] = 0x7F
+    pa.pa_swap_blocks(case.k_pools, case.v_pools, host, in_ids, pa.PA_SWAP_IN, staging=staging)
+    torch.cuda.synchronize()
+    assert oracle.load().swap_blocks(kps, vps, exp, in_ids, block_bytes=bb, direction="in") == 0
+    for l in range(L):
+        np.testing.assert_array_equal(_u8(case.k_pools[l]).reshape(case.num_blocks, -1)[in_ids],
+                                      kps[l].reshape(case.num_blocks, -1)[in_ids])
+        np.testing.assert_array_equal(_u8(case.v_pools[l]).reshape(case.num_blocks, -1)[in_ids],
+                                      vps[l].reshape(case.num_blocks, -1)[in_ids])
+    bt = case.block_tables.clone()
+    bt[victim, :n] = torch.from_numpy(in_ids).cuda()
+    after = gpu_decode(case, block_tables=bt)
+    assert torch.equal(after[victim], before[victim]), "resumed decode must be bit-identical"
+
+
+def test_swap_rejects_pageable_and_bad_ids():
+    spec = synth.SPECS["toy"]
+    case = synth.make_case(spec, seed=2).to("cuda")
+    bb = case.block_bytes
+    pageable = torch.zeros(2 * 2 * bb, dtype=torch.uint8)
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_swap_blocks([case.k_pool], [case.v_pool], pageable, [0, 1], pa.PA_SWAP_OUT)
+    assert e.value.status == pa.PA_EINVAL
+    pinned = pageable.pin_memory()
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_swap_blocks([case.k_pool], [case.v_pool], pinned, [0, 9], pa.PA_SWAP_OUT)
+    assert e.value.status == pa.PA_EINVAL
