@@ -7,19 +7,26 @@
 // equals ordinary attention. "Continuous Batching and PagedAttention", section "The block table
 // is a page table": the kernel gathers through the table instead of striding.
 //
-// GB300 design (one CTA per (context split, kv head, sequence)):
-//   * warp 0 is the producer: one lane walks the split's block-table slice (read once into shared
-//     memory, out-of-pool ids masked and flagged) and issues 2-D TMA tensor copies of each
-//     (block, kv head) tile of K and V into a ring of shared-memory stages, 128-byte swizzled,
-//     completing on per-stage mbarriers;
-//   * warps 1..4 are consumers: stage t is consumed by warp t % 4, each with its own online
-//     softmax state (running max in log2 units, running sum, fp32 accumulator);
-//   * group size G <= 2: warp-shuffle dot products (CUDA cores), one token row per lane group;
-//     G >= 4: the GQA group makes each 16-token tile a small dense contraction, done with
-//     mma.sync m16n8k16 (S^T = K Q^T with the G query heads as the N dimension, then
-//     O^T += V^T P^T), fp32 accumulation;
-//   * the four consumer states are merged in shared memory; one split writes the output
-//     directly, several splits write fp32 partials that pa_reduce_kernel combines.
+// GB300 design: a persistent kernel, one CTA of 13 warps per SM.
+//   * Work items are (sequence, kv head, context split) in sequence order; CTAs take the next
+//     item from a global counter, so the items of sequences that share prompt blocks run at the
+//     same time on different SMs and the shared blocks are served from L2.
+//   * Warp 0 schedules: it keeps up to 4 items queued in shared memory -- descriptor, the
+//     item's block-table slice (one coalesced load, out-of-pool ids masked and flagged) and the
+//     group's queries (one bulk copy).
+//   * Warps 1..4 produce: tile g of the CTA's tile sequence is issued by warp 1 + g % 4 as 2-D
+//     TMA tensor copies of each (block, kv head) tile of K and V into a ring of shared-memory
+//     stages (128-byte swizzle) completing on mbarriers. Several issuing warps are needed: one
+//     warp's in-order stream of copies reaches only a fraction of an SM's share of HBM
+//     bandwidth. The ring runs across item boundaries, so HBM traffic does not stop between items.
+//   * Warps 5..12 consume: tile t of an item goes to consumer t % 8, each keeping its own
+//     online-softmax state (running max in log2 units, running sum, fp32 accumulator).
+//     Group size G <= 2: warp-shuffle dot products on the CUDA cores. G >= 4: the GQA group makes
+//     each 16-token tile a small dense contraction, done with mma.sync m16n8k16
+//     (S^T = K Q^T with the G query heads as the N dimension, then O^T += V^T P^T).
+//   * At the end of an item the consumer states are merged in shared memory; an item that covers
+//     its sequence's whole context writes the output, otherwise fp32 partials that
+//     pa_reduce_kernel combines.
 #pragma once
 
 #include "pa_device.cuh"
@@ -28,9 +35,14 @@ namespace pa {
 
 enum KvKind { kKvF16 = 0, kKvBF16 = 1, kKvE4M3 = 2 };
 
-constexpr int kConsumerWarps = 4;
-constexpr int kDecodeThreads = 32 * (1 + kConsumerWarps);
-constexpr int kMaxStages = 16;
+constexpr int kProducerWarps = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kDecodeThreads = 32 * (1 + kProducerWarps + kConsumerWarps);
+constexpr int kMaxStages = 32;
+constexpr int kItemSlots = 4;          // work items queued ahead by the scheduler warp
+constexpr int kMaxItemBlocks = 256;    // block-table entries of one work item
+constexpr int kMaxSeqsPerLaunch = 4096;
+constexpr int kScanSlots = kDecodeThreads;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -38,20 +50,36 @@ struct DecodeParams {
   void* out;
   const int32_t* block_tables;
   const int32_t* ctx_lens;
-  float* part_o;    // [num_seqs][num_q_heads][max_splits][D] unnormalised, v_scale applied
-  float2* part_ml;  // [num_seqs][num_q_heads][max_splits] (max score in log2 units, weight sum)
+  float* part_o;        // [num_seqs][num_q_heads][max_splits][D] unnormalised, v_scale applied
+  float2* part_ml;      // [num_seqs][num_q_heads][max_splits] (max score in log2 units, weight sum)
+  unsigned long long* counters;  // [0] next work item, [1] CTAs finished (launch-id tagged)
+  uint32_t launch_id;
   int32_t* err;
   int num_seqs, num_q_heads, num_kv_heads;
   int block_size, log2_block, num_blocks, max_blocks, max_ctx;
-  int split_tokens;   // tokens per split, a multiple of max(16, block_size)
-  int max_splits;     // ceil(max_ctx / split_tokens)
-  int stages;         // shared-memory ring depth, a multiple of kConsumerWarps
-  int region_stride;  // bytes of one 128-byte-wide column region of one block in a stage
-  int stage_bytes;    // bytes of K (or V) in one stage
-  int ctl_offset;     // offset of the barriers / table area from the aligned smem base
-  float score_scale;  // scale * k_scale * log2(e)
+  int split_tokens;     // tokens per work item, a multiple of max(16, block_size)
+  int max_splits;       // ceil(max_ctx / split_tokens)
+  int stages;           // shared-memory ring depth, a multiple of kConsumerWarps
+  int region_stride;    // bytes of one 128-byte-wide column region of one block in a stage
+  int stage_bytes;      // bytes of K (or V) in one stage
+  // byte offsets from the 1024-aligned shared-memory base
+  int off_merge, off_q, off_bar, off_meta, off_items, off_tbl, off_scan;
+  int tbl_stride;       // block-table entries per item slot
+  float score_scale;    // scale * k_scale * log2(e)
   float v_scale;
-  int q_bf16;         // query / output dtype for E4M3 KV (16-bit KV: same as the KV dtype)
+  int q_bf16;           // query / output dtype is bf16 (else f16)
+};
+
+// Work item handed from the scheduler warp to the producers and consumers in shared memory.
+struct ItemDesc {
+  int seq;      // -1: no more work
+  int kvh;
+  int split;
+  int nsplit;   // splits of this sequence
+  int ntiles;   // ring stages of this item
+  int tok0;     // first token of the item
+  int tok_end;  // one past its last token
+  int nblk;     // blocks of the item (their physical ids, or -1, follow in the table slot)
 };
 
 template <int KV, int D>
@@ -62,10 +90,6 @@ struct Geom {
   static constexpr int kColsPerRegion = 128 / kElt;
 };
 
-template <int G, int D>
-struct MergeSize {
-  static constexpr int kBytes = kConsumerWarps * G * D * 4 + kConsumerWarps * G * 8;
-};
 
 // Byte offset inside a stage tensor of (token row r of the stage, 16-byte chunk c of the row),
 // matching the TMA 128-byte swizzle (chunk index XOR row-in-8) of each 1024-aligned region.
@@ -111,30 +135,24 @@ struct Consumer<KV, D, G, false> {
   float m[G], l[G];
   int grp, ci;
 
-  __device__ void init(const DecodeParams& p, int seq, int kvh, int lane) {
+  // qs: the group's G query rows (G x D, f16 or bf16) staged in shared memory.
+  __device__ void init(const uint16_t* qs, bool qbf, int lane) {
     grp = lane / kCpr;
     ci = lane % kCpr;
     for (int h = 0; h < G; ++h) {
-      const size_t row = (static_cast<size_t>(seq) * p.num_q_heads + kvh * G + h) * D;
-      const int d0 = ci * kE;
-      load_q(p, row + d0, q[h]);
+      const uint16_t* row = qs + h * D + ci * kE;
+      for (int e = 0; e < kE; e += 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + e);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = qbf ? bf16x2_to_float2(w[k]) : f16x2_to_float2(w[k]);
+          q[h][e + 2 * k] = f.x;
+          q[h][e + 2 * k + 1] = f.y;
+        }
+      }
       for (int e = 0; e < kE; ++e) acc[h][e] = 0.f;
       m[h] = -INFINITY;
       l[h] = 0.f;
-    }
-  }
-
-  __device__ static void load_q(const DecodeParams& p, size_t idx, float (&dst)[kE]) {
-    const bool qbf = (KV == kKvE4M3) ? (p.q_bf16 != 0) : (KV == kKvBF16);
-    const uint16_t* qp = static_cast<const uint16_t*>(p.q) + idx;
-    for (int e = 0; e < kE; e += 8) {
-      const uint4 v = *reinterpret_cast<const uint4*>(qp + e);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = qbf ? bf16x2_to_float2(w[k]) : f16x2_to_float2(w[k]);
-        dst[e + 2 * k] = f.x;
-        dst[e + 2 * k + 1] = f.y;
-      }
     }
   }
 
@@ -250,19 +268,17 @@ struct Consumer<KV, D, G, true> {
   float qexp;  // 2^-e of the query pre-scaling (E4M3 path), else 1
   int g, t4;
 
-  __device__ void init(const DecodeParams& p, int seq, int kvh, int lane) {
+  // qs: the group's G query rows (G x D, f16 or bf16) staged in shared memory.
+  __device__ void init(const uint16_t* qs, bool qbf, int lane) {
     g = lane >> 2;
     t4 = lane & 3;
-    const size_t head0 = static_cast<size_t>(seq) * p.num_q_heads + kvh * G;
     qexp = 1.f;
     if constexpr (kFp8) {
       // Queries go to f16 for the f16 MMA. A power-of-two pre-scale 2^e puts the largest |q|
       // of the group in [2^14, 2^15): exact for every bf16 value in f16's normal range.
-      const bool qbf = p.q_bf16 != 0;
-      const uint16_t* qp = static_cast<const uint16_t*>(p.q) + head0 * D;
       float amax = 0.f;
       for (int i = lane; i < G * D; i += 32) {
-        const uint16_t b = qp[i];
+        const uint16_t b = qs[i];
         const float v = qbf ? __uint_as_float(static_cast<uint32_t>(b) << 16)
                             : __half2float(*reinterpret_cast<const __half*>(&b));
         amax = fmaxf(amax, fabsf(v));
@@ -278,25 +294,24 @@ struct Consumer<KV, D, G, true> {
           for (int r = 0; r < 2; ++r) {
             // logical k = 2*t4 + 8*r + {0,1} of k-step j <-> d = 32*t4 + 4*j + 2*r + {0,1}
             const int d = 32 * t4 + 4 * j + 2 * r;
-            float a = 0.f, b = 0.f;
+            float x = 0.f, y = 0.f;
             if (n < G) {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(qp + n * D + d);
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(qs + n * D + d);
               const float2 f = qbf ? bf16x2_to_float2(w) : f16x2_to_float2(w);
-              a = f.x * up;
-              b = f.y * up;
+              x = f.x * up;
+              y = f.y * up;
             }
-            qf[nt][j][r] = pack2<false>(a, b);
+            qf[nt][j][r] = pack2<false>(x, y);
           }
         }
       }
     } else {
-      const uint16_t* qp = static_cast<const uint16_t*>(p.q) + head0 * D;
       for (int nt = 0; nt < kNT; ++nt) {
         const int n = nt * 8 + g;
         for (int j = 0; j < kK; ++j) {
           for (int r = 0; r < 2; ++r) {
             const int d = 16 * j + 8 * r + 2 * t4;
-            qf[nt][j][r] = n < G ? *reinterpret_cast<const uint32_t*>(qp + n * D + d) : 0u;
+            qf[nt][j][r] = n < G ? *reinterpret_cast<const uint32_t*>(qs + n * D + d) : 0u;
           }
         }
       }
@@ -501,183 +516,348 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, bool b
     static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
+__device__ __forceinline__ int phs_of(const int (&phs)[4], int b) {
+  return b == 0 ? phs[0] : b == 1 ? phs[1] : b == 2 ? phs[2] : phs[3];
+}
+
 template <int KV, int D, int G>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 1)
     pa_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeParams p) {
   using Gm = Geom<KV, D>;
   constexpr bool kMma = G >= 4;
-  const bool out_bf16 = KV == kKvE4M3 ? (p.q_bf16 != 0) : (KV == kKvBF16);
+  constexpr int kConsumerThreads = kConsumerWarps * 32;
+  constexpr int kFirstConsumer = 1 + kProducerWarps;  // warp index of consumer 0
+  const bool qbf = p.q_bf16 != 0;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* base_ptr = smem_raw + (base - raw);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(base_ptr + p.ctl_offset);  // full[16], empty[16]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar + 2 * kMaxStages);
-  int* tbl = reinterpret_cast<int*>(bar + 2 * kMaxStages) + 4;
-  float* mrg_o = reinterpret_cast<float*>(base_ptr);
-  float2* mrg_ml = reinterpret_cast<float2*>(base_ptr + kConsumerWarps * G * D * 4);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // ring of stages starts here
+  uint8_t* bp = smem_raw + (base - raw);
+  float* mrg_o = reinterpret_cast<float*>(bp + p.off_merge);
+  float2* mrg_ml = reinterpret_cast<float2*>(bp + p.off_merge + kConsumerWarps * G * D * 4);
+  uint16_t* qbuf = reinterpret_cast<uint16_t*>(bp + p.off_q);  // [kItemSlots][G * D]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(bp + p.off_bar);
+  uint64_t* full = bar;                       // [kMaxStages] stage landed
+  uint64_t* empty = bar + kMaxStages;         // [kMaxStages] stage consumed
+  uint64_t* qfull = bar + 2 * kMaxStages;     // [kItemSlots] item descriptor, table, queries ready
+  uint64_t* qempty = qfull + kItemSlots;      // [kItemSlots] slot released by producers + consumers
+  uint32_t* meta = reinterpret_cast<uint32_t*>(bp + p.off_meta);     // [kMaxStages] valid tokens
+  ItemDesc* items = reinterpret_cast<ItemDesc*>(bp + p.off_items);  // [kItemSlots]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(items + kItemSlots);
+  int* tbl = reinterpret_cast<int*>(bp + p.off_tbl);      // [kItemSlots][tbl_stride]
+  int* prefix = reinterpret_cast<int*>(bp + p.off_scan);  // [num_seqs + 1]
+  int* partial = prefix + p.num_seqs + 1;                  // [kScanSlots]
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
-  const int B = p.block_size;
-  const int L = __ldg(p.ctx_lens + seq);
-  const size_t out_head0 = static_cast<size_t>(seq) * p.num_q_heads + kvh * G;
-
-  const bool bad_len = L < 0 || L > p.max_ctx || L > p.max_blocks * B;
-  if (bad_len || L == 0) {
-    if (split == 0) {
-      if (bad_len && threadIdx.x == 0) flag_error(p.err, kErrCtxLen);
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x) store_out(p.out, out_head0 * D + i, 0.f, out_bf16);
-    }
-    return;
-  }
-  const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
-  if (split >= nsplit) return;
-
-  const int tok0 = split * p.split_tokens;
-  const int tok_end = min(L, tok0 + p.split_tokens);
-  const int blk0 = tok0 >> p.log2_block;
-  const int nblk = ((tok_end - 1) >> p.log2_block) - blk0 + 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int N = p.num_seqs, Hkv = p.num_kv_heads, B = p.block_size, S = p.split_tokens;
   const int st_tokens = max(16, B);
-  const int bps = st_tokens >> p.log2_block;
-  const int tiles = (tok_end - tok0 + st_tokens - 1) / st_tokens;
 
-  const int32_t* trow = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
-  for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
-    int ph = __ldg(trow + i);
-    if (ph < 0 || ph >= p.num_blocks) {
-      flag_error(p.err, kErrBlockId);
-      ph = -1;
+  // ---- prologue: work items per sequence (kv heads x splits) and their prefix sums
+  {
+    const int per = (N + kDecodeThreads - 1) / kDecodeThreads;
+    const int s0 = min(N, tid * per), s1 = min(N, s0 + per);
+    int local = 0;
+    for (int s = s0; s < s1; ++s) {
+      const int L = __ldg(p.ctx_lens + s);
+      const bool bad = L < 0 || L > p.max_ctx || L > p.max_blocks * B;
+      const int cnt = (bad || L == 0) ? 0 : ((L + S - 1) / S) * Hkv;
+      prefix[s] = cnt;
+      local += cnt;
+      if ((bad || L == 0) && (s % gridDim.x) == blockIdx.x) {
+        if (bad) flag_error(p.err, kErrCtxLen);
+        const size_t row0 = static_cast<size_t>(s) * p.num_q_heads * D;
+        for (int i = 0; i < p.num_q_heads * D; ++i) store_out(p.out, row0 + i, 0.f, qbf);
+      }
     }
-    tbl[i] = ph;
-  }
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(smem_addr(bar + s), 1);
-      mbar_init(smem_addr(bar + kMaxStages + s), 1);
+    partial[tid] = local;
+    if (tid == 0) {
+      *abort_flag = 0;
+      for (int s = 0; s < p.stages; ++s) {
+        mbar_init(smem_addr(full + s), 1);
+        mbar_init(smem_addr(empty + s), 1);
+      }
+      for (int b = 0; b < kItemSlots; ++b) {
+        mbar_init(smem_addr(qfull + b), 1);
+        mbar_init(smem_addr(qempty + b), kProducerWarps + kConsumerWarps);
+      }
+      fence_barrier_init();
     }
-    fence_barrier_init();
+    __syncthreads();
+    if (tid == 0) {
+      int run = 0;
+      for (int i = 0; i < kDecodeThreads; ++i) {
+        const int c = partial[i];
+        partial[i] = run;
+        run += c;
+      }
+      prefix[N] = run;
+    }
+    __syncthreads();
+    int run = partial[tid];
+    for (int s = s0; s < s1; ++s) {
+      const int c = prefix[s];
+      prefix[s] = run;
+      run += c;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-
-  const uint32_t stage0 = base;  // stage s: K at stage0 + 2*s*stage_bytes, V right after
+  const int total_items = prefix[N];
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
-      const uint64_t pol = policy_evict_normal();
-      const uint32_t tile_bytes = static_cast<uint32_t>(2 * Gm::kRegions * B * 128);
-      int issued = 0;
-      bool aborted = false;
-      for (int t = 0; t < tiles; ++t) {
-        const int s = t % p.stages;
-        if (t >= p.stages) {
-          if (!mbar_wait_bounded(smem_addr(bar + kMaxStages + s), ((t / p.stages) - 1) & 1)) {
-            flag_error(p.err, kErrTimeout);
-            *abort_flag = 1;
-            aborted = true;
-            break;
-          }
+    // ------------------------------------------------------------------ scheduler warp
+    // Takes items from the global counter in sequence order and fills the item slots:
+    // descriptor, the item's block-table slice (validated) and, by bulk copy, its queries.
+    const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it % kItemSlots;
+      if (it >= kItemSlots &&
+          !mbar_wait_bounded(smem_addr(qempty + slot), ((it / kItemSlots) - 1) & 1)) {
+        if (lane == 0) {
+          flag_error(p.err, kErrTimeout);
+          *abort_flag = 1;
         }
-        if (*abort_flag) {
-          aborted = true;
-          break;
-        }
-        uint32_t bytes = 0;
-        for (int b = 0; b < bps; ++b) {
-          const int j = t * bps + b;
-          if (j < nblk && tbl[j] >= 0) bytes += tile_bytes;
-        }
-        const uint32_t full = smem_addr(bar + s);
-        mbar_arrive_expect_tx(full, bytes);
-        const uint32_t kdst = stage0 + static_cast<uint32_t>(2 * s * p.stage_bytes);
-        const uint32_t vdst = kdst + static_cast<uint32_t>(p.stage_bytes);
-        for (int b = 0; b < bps; ++b) {
-          const int j = t * bps + b;
-          if (j >= nblk || tbl[j] < 0) continue;
-          const int y = (tbl[j] * p.num_kv_heads + kvh) * B;
-          for (int c = 0; c < Gm::kRegions; ++c) {
-            const uint32_t off = static_cast<uint32_t>((b * Gm::kRegions + c) * p.region_stride);
-            tma_load_2d(kdst + off, &kmap, c * Gm::kColsPerRegion, y, full, pol);
-            tma_load_2d(vdst + off, &vmap, c * Gm::kColsPerRegion, y, full, pol);
-          }
-        }
-        issued = t + 1;
+        break;
       }
-      if (aborted) {
-        // nothing may still be landing in shared memory when the CTA exits
-        for (int t = max(0, issued - p.stages); t < issued; ++t)
-          mbar_wait_bounded(smem_addr(bar + (t % p.stages)), (t / p.stages) & 1);
+      int item = 0, seq = 0;
+      if (lane == 0) {
+        item = static_cast<int>(fetch_ticket(p.counters, p.launch_id));
+        if (item < total_items) {
+          int lo = 0, hi = N - 1;  // largest s with prefix[s] <= item
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+          }
+          seq = lo;
+        }
+      }
+      item = __shfl_sync(0xffffffffu, item, 0);
+      seq = __shfl_sync(0xffffffffu, seq, 0);
+      ItemDesc& d = items[slot];
+      if (item >= total_items || *abort_flag) {
+        if (lane == 0) {
+          d.seq = -1;
+          mbar_arrive(smem_addr(qfull + slot));
+        }
+        break;
+      }
+      const int L = __ldg(p.ctx_lens + seq);
+      const int nsplit = (L + S - 1) / S;
+      const int li = item - prefix[seq];
+      const int kvh = li / nsplit, split = li % nsplit;
+      const int tok0 = split * S, tok_end = min(L, tok0 + S);
+      const int blk0 = tok0 >> p.log2_block;
+      const int nblk = ((tok_end - 1) >> p.log2_block) - blk0 + 1;
+      const int32_t* trow = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
+      int* slot_tbl = tbl + slot * p.tbl_stride;
+      for (int j = lane; j < nblk; j += 32) {
+        int ph = __ldg(trow + j);
+        if (ph < 0 || ph >= p.num_blocks) {
+          flag_error(p.err, kErrBlockId);
+          ph = -1;
+        }
+        slot_tbl[j] = ph;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        d.seq = seq;
+        d.kvh = kvh;
+        d.split = split;
+        d.nsplit = nsplit;
+        d.ntiles = (tok_end - tok0 + st_tokens - 1) / st_tokens;
+        d.tok0 = tok0;
+        d.tok_end = tok_end;
+        d.nblk = nblk;
+        const uint32_t qf = smem_addr(qfull + slot);
+        mbar_arrive_expect_tx(qf, qbytes);
+        bulk_copy_g2s(smem_addr(qbuf + slot * G * D),
+                      static_cast<const uint16_t*>(p.q) +
+                          (static_cast<size_t>(seq) * p.num_q_heads + kvh * G) * D,
+                      qbytes, qf);
       }
     }
-    return;
-  }
-
-  // -------------------------------------------------------------------- consumers
-  const int cw = warp - 1;
-  Consumer<KV, D, G, kMma> c;
-  c.init(p, seq, kvh, lane);
-  float score_scale = p.score_scale;
-  if constexpr (kMma && KV == kKvE4M3) score_scale *= c.qexp;
-
-  for (int t = cw; t < tiles; t += kConsumerWarps) {
-    const int s = t % p.stages;
-    if (!mbar_wait_bounded(smem_addr(bar + s), (t / p.stages) & 1)) {
+  } else if (warp <= kProducerWarps) {
+    // ------------------------------------------------------------------ producer warps
+    // Producer pw issues the tiles g = pw (mod kProducerWarps) of the CTA's tile sequence.
+    // Several issuing warps keep enough copies in flight: one warp alone streams far below
+    // the per-SM share of HBM bandwidth.
+    const int pw = warp - 1;
+    const uint64_t pol = policy_evict_normal();
+    if (lane == 0 && pw == 0) {
+      prefetch_tensormap(&kmap);
+      prefetch_tensormap(&vmap);
+    }
+    const uint32_t tile_bytes = static_cast<uint32_t>(2 * Gm::kRegions * B * 128);
+    const int bps = st_tokens >> p.log2_block;  // blocks per stage (1, 2 or 4)
+    uint32_t g0 = 0;                            // CTA tile index of the item's first tile
+    bool ok = true;
+    uint32_t issued_last = 0, any = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it % kItemSlots;
+      if (!mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1)) {
+        ok = false;
+        break;
+      }
+      const ItemDesc d = items[slot];
+      if (d.seq < 0) break;
+      const int* slot_tbl = tbl + slot * p.tbl_stride;
+      int t = (pw - static_cast<int>(g0 % kProducerWarps) + kProducerWarps) % kProducerWarps;
+      for (; t < d.ntiles; t += kProducerWarps) {
+        const uint32_t g = g0 + t;
+        const int s = static_cast<int>(g % p.stages);
+        if (g >= static_cast<uint32_t>(p.stages) &&
+            !mbar_wait_bounded(smem_addr(empty + s), ((g / p.stages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        uint32_t valid = 0, bytes = 0;
+        int phs[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          phs[b] = -1;
+          const int j = t * bps + b;
+          if (b < bps && j < d.nblk) {
+            const int ph = slot_tbl[j];
+            if (ph >= 0) {
+              phs[b] = ph;
+              bytes += tile_bytes;
+              const int r0 = b * B;
+              const int n = min(B, d.tok_end - (d.tok0 + t * st_tokens + r0));
+              valid |= (n >= 32 ? 0xffffffffu : ((1u << n) - 1u)) << r0;
+            }
+          }
+        }
+        const uint32_t fb = smem_addr(full + s);
+        if (lane == 0) {
+          meta[s] = valid;
+          mbar_arrive_expect_tx(fb, bytes);
+        }
+        __syncwarp();
+        {  // one lane per copy: (block b, K|V, column region c)
+          constexpr int kOps = 2 * Gm::kRegions;
+          const int b = lane / kOps, kv = (lane / Gm::kRegions) & 1, c = lane % Gm::kRegions;
+          if (b < bps && phs_of(phs, b) >= 0) {
+            const uint32_t off = static_cast<uint32_t>(2 * s * p.stage_bytes + kv * p.stage_bytes +
+                                                       (b * Gm::kRegions + c) * p.region_stride);
+            tma_load_2d(base + off, kv ? &vmap : &kmap, c * Gm::kColsPerRegion,
+                        (phs_of(phs, b) * Hkv + d.kvh) * B, fb, pol);
+          }
+        }
+        issued_last = g;
+        any = 1;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(qempty + slot));
+      if (!ok) break;
+      g0 += d.ntiles;
+    }
+    if (!ok) {
       if (lane == 0) {
         flag_error(p.err, kErrTimeout);
         *abort_flag = 1;
       }
-      break;
-    }
-    const uint32_t ks = stage0 + static_cast<uint32_t>(2 * s * p.stage_bytes);
-    const uint32_t vs = ks + static_cast<uint32_t>(p.stage_bytes);
-    for (int sub = 0; sub < st_tokens; sub += 16) {
-      // validity of the 16 tokens of this tile: inside the context and in a usable block
-      const int rt = t * st_tokens + sub + (lane & 15);
-      const bool ok = (tok0 + rt < tok_end) && tbl[min(rt >> p.log2_block, nblk - 1)] >= 0;
-      const uint32_t valid = __ballot_sync(0xffffffffu, ok && lane < 16) & 0xffffu;
-      if (valid == 0) continue;
-      c.tile(p, ks, vs, sub, valid, score_scale);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(bar + kMaxStages + s));
-    if (*abort_flag) break;
-  }
-
-  // merge the consumer warps (the stage ring is reused once every consumer is done with it)
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-  c.publish(mrg_o, mrg_ml, cw, lane);
-  asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-
-  const int ctid = threadIdx.x - 32;
-  const bool single = nsplit == 1;
-  for (int idx = ctid; idx < G * D; idx += kConsumerWarps * 32) {
-    const int n = idx / D, d = idx % D;
-    float mstar = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) mstar = fmaxf(mstar, mrg_ml[w * G + n].x);
-    float num = 0.f, den = 0.f;
-    if (mstar != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float2 ml = mrg_ml[w * G + n];
-        const float wgt = ex2(ml.x - mstar);
-        num = fmaf(wgt, mrg_o[(w * G + n) * D + d], num);
-        den = fmaf(wgt, ml.y, den);
+      // nothing this warp issued may still be landing in shared memory when the CTA exits
+      if (any) {
+        const uint32_t span = static_cast<uint32_t>(p.stages);
+        const uint32_t from = issued_last >= span ? issued_last - span + 1 : 0u;
+        for (uint32_t g = from; g <= issued_last; ++g)
+          if (g % kProducerWarps == static_cast<uint32_t>(pw))
+            mbar_wait_bounded(smem_addr(full + (g % p.stages)), (g / p.stages) & 1);
       }
     }
-    if (single) {
-      const float v = den > 0.f ? num / den * p.v_scale : 0.f;
-      store_out(p.out, (out_head0 + n) * D + d, v, out_bf16);
-    } else {
-      const size_t slot = (out_head0 + n) * p.max_splits + split;
-      p.part_o[slot * D + d] = num * p.v_scale;
-      if (d == 0) p.part_ml[slot] = make_float2(mstar, den);
+  } else {
+    // ------------------------------------------------------------------ consumer warps
+    const int cw = warp - kFirstConsumer;
+    const int ctid = tid - kFirstConsumer * 32;
+    Consumer<KV, D, G, kMma> c;
+    uint32_t g0 = 0;
+    for (uint32_t it = 0;; ++it) {
+      const int slot = it % kItemSlots;
+      const bool got = mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1);
+      if (bar_or(kConsumerThreads, !got)) {  // every consumer warp leaves together
+        if (ctid == 0) {
+          flag_error(p.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      const ItemDesc d = items[slot];
+      if (d.seq < 0) break;
+      c.init(qbuf + slot * G * D, qbf, lane);
+      float score_scale = p.score_scale;
+      if constexpr (kMma && KV == kKvE4M3) score_scale *= c.qexp;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(qempty + slot));
+
+      bool ok = true;
+      for (int t = cw; t < d.ntiles; t += kConsumerWarps) {
+        const uint32_t g = g0 + t;
+        const int s = static_cast<int>(g % p.stages);
+        if (!mbar_wait_bounded(smem_addr(full + s), (g / p.stages) & 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t valid = meta[s];
+        const uint32_t ks = base + static_cast<uint32_t>(2 * s * p.stage_bytes);
+        const uint32_t vs = ks + static_cast<uint32_t>(p.stage_bytes);
+        for (int sub = 0; sub < st_tokens; sub += 16) {
+          const uint32_t v16 = (valid >> sub) & 0xffffu;
+          if (v16) c.tile(p, ks, vs, sub, v16, score_scale);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(empty + s));
+      }
+
+      // merge the consumer warps' states for this item and write it out
+      c.publish(mrg_o, mrg_ml, cw, lane);
+      bar_sync(1, kConsumerThreads);
+      const size_t head0 = static_cast<size_t>(d.seq) * p.num_q_heads + d.kvh * G;
+      for (int idx = ctid; idx < G * D; idx += kConsumerThreads) {
+        const int n = idx / D, dd = idx % D;
+        float mstar = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) mstar = fmaxf(mstar, mrg_ml[w * G + n].x);
+        float num = 0.f, den = 0.f;
+        if (mstar != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float2 ml = mrg_ml[w * G + n];
+            const float wgt = ex2(ml.x - mstar);
+            num = fmaf(wgt, mrg_o[(w * G + n) * D + dd], num);
+            den = fmaf(wgt, ml.y, den);
+          }
+        }
+        if (d.nsplit == 1) {
+          store_out(p.out, (head0 + n) * D + dd, den > 0.f ? num / den * p.v_scale : 0.f, qbf);
+        } else {
+          const size_t slot_i = (head0 + n) * p.max_splits + d.split;
+          p.part_o[slot_i * D + dd] = num * p.v_scale;
+          if (dd == 0) p.part_ml[slot_i] = make_float2(mstar, den);
+        }
+      }
+      if (bar_or(kConsumerThreads, !ok || *abort_flag)) {
+        if (ctid == 0) {
+          flag_error(p.err, kErrTimeout);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      g0 += d.ntiles;
+    }
+  }
+
+  // ---- the last CTA to finish clears the work counters for the next launch
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t done = fetch_ticket(p.counters + 1, p.launch_id);
+    if (done == gridDim.x - 1) {
+      atomicExch(p.counters, 0ull);
+      atomicExch(p.counters + 1, 0ull);
     }
   }
 }

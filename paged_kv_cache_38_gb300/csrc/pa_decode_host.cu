@@ -2,6 +2,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "pa_decode.cuh"
@@ -160,9 +161,6 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   pl.stage_tokens = std::max(16, B);
   pl.region_stride = std::max(B * 128, 1024);
   pl.stage_bytes = (pl.stage_tokens / B) * pl.regions * pl.region_stride;
-  int stages = 65536 / (2 * pl.stage_bytes);
-  stages = (stages / kConsumerWarps) * kConsumerWarps;
-  pl.stages = std::min(kMaxStages, std::max(kConsumerWarps, stages));
 
   const int stok = pl.stage_tokens;
   if (a.split_tokens > 0) {
@@ -172,51 +170,84 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
     }
     pl.split_tokens = a.split_tokens;
   } else {
-    // about 256 KiB of K+V per split, fewer tokens when the grid would not fill the GPU
+    // work items of about 256 KiB of K+V, fewer tokens when there would be too few items
     int tokens = (256 * 1024) / (2 * D * pl.elt);
     const long long units = static_cast<long long>(a.num_seqs) * a.num_kv_heads;
     const int sms = sm_count > 0 ? sm_count : 148;
-    while (tokens > 4 * stok && units * ((a.max_ctx_len + tokens - 1) / tokens) < 4LL * sms)
+    while (tokens > 4 * stok && units * ((a.max_ctx_len + tokens - 1) / tokens) < 8LL * sms)
       tokens /= 2;
     pl.split_tokens = std::max(stok, (tokens / stok) * stok);
   }
   pl.max_splits = std::max(1, (a.max_ctx_len + pl.split_tokens - 1) / pl.split_tokens);
-  if (pl.max_splits > 65535) {
-    msg = "too many context splits; raise split_tokens";
+  pl.seqs_per_launch = std::max(1, std::min(a.num_seqs, kMaxSeqsPerLaunch));
+
+  // shared memory: [ring][merge][queries][barriers][stage meta][items + flag][tables][scan]
+  const int tbl_entries = pl.split_tokens / B + 1;
+  if (tbl_entries > kMaxItemBlocks) {
+    msg = "split_tokens / block_size must be below 256";
     return PA_EINVAL;
   }
-  const int merge = kConsumerWarps * group * D * 4 + kConsumerWarps * group * 8;
-  pl.ctl_offset = ((std::max(pl.stages * 2 * pl.stage_bytes, merge) + 15) / 16) * 16;
-  const int table_entries = pl.split_tokens / B + 1;
-  pl.smem_bytes = 1024 + pl.ctl_offset + 2 * kMaxStages * 8 + 16 + table_entries * 4;
-  if (pl.smem_bytes > 227 * 1024) {
-    msg = "split_tokens too large for the shared-memory block-table slice";
-    return PA_EINVAL;
+  auto up = [](size_t x, size_t al) { return (x + al - 1) / al * al; };
+  const size_t merge = static_cast<size_t>(kConsumerWarps) * group * D * 4 +
+                       static_cast<size_t>(kConsumerWarps) * group * 8;
+  const size_t qbytes = static_cast<size_t>(kItemSlots) * group * D * 2;
+  const size_t bars = (2 * kMaxStages + 2 * kItemSlots) * 8;
+  const size_t meta = kMaxStages * 4;
+  const size_t items = kItemSlots * sizeof(ItemDesc) + 16;
+  pl.tbl_stride = ((tbl_entries + 3) / 4) * 4;
+  const size_t tbls = static_cast<size_t>(kItemSlots) * pl.tbl_stride * 4;
+  const size_t scan = (static_cast<size_t>(pl.seqs_per_launch) + 1 + kScanSlots) * 4;
+  const size_t fixed = up(merge, 16) + up(qbytes, 128) + bars + meta + items + tbls + up(scan, 16);
+  const size_t limit = 227 * 1024 - 1024;  // opt-in maximum per CTA, minus alignment slack
+  if (fixed + 2 * static_cast<size_t>(pl.stage_bytes) * 8 > limit) {
+    msg = "shared-memory budget exceeded (too many sequences per launch for this group size)";
+    return PA_EUNSUPPORTED;
   }
-  if (pl.max_splits > 1) {
-    const size_t slots = static_cast<size_t>(a.num_seqs) * a.num_q_heads * pl.max_splits;
-    pl.workspace = ((slots * D * 4 + 255) / 256) * 256 + slots * 8;
-  } else {
-    pl.workspace = 0;
-  }
+  // The ring depth must be a multiple of the consumer and producer warp counts: two tiles that
+  // share a stage then always belong to the same consumer warp and the same producer warp, which
+  // handle them in order, so no mbarrier parity wait can see an older phase of the stage.
+  static_assert(kConsumerWarps % kProducerWarps == 0, "ring depth rule");
+  size_t depth = std::min<size_t>(kMaxStages, (limit - fixed) / (2 * pl.stage_bytes));
+  depth = (depth / kConsumerWarps) * kConsumerWarps;
+  pl.stages = static_cast<int>(depth);
+  size_t off = static_cast<size_t>(pl.stages) * 2 * pl.stage_bytes;
+  pl.off_merge = static_cast<int>(off);
+  off = up(off + merge, 128);
+  pl.off_q = static_cast<int>(off);
+  off = up(off + qbytes, 16);
+  pl.off_bar = static_cast<int>(off);
+  off += bars;
+  pl.off_meta = static_cast<int>(off);
+  off += meta;
+  pl.off_items = static_cast<int>(off);
+  off += items;
+  pl.off_tbl = static_cast<int>(off);
+  off += tbls;
+  pl.off_scan = static_cast<int>(off);
+  off += scan;
+  pl.smem_bytes = 1024 + off;
+
+  const size_t slots = static_cast<size_t>(pl.seqs_per_launch) * a.num_q_heads * pl.max_splits;
+  pl.partial_o_bytes = pl.max_splits > 1 ? up(slots * D * 4, 256) : 0;
+  pl.workspace = 256 + (pl.max_splits > 1 ? pl.partial_o_bytes + slots * 8 : 0);
   return PA_OK;
 }
 
 pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& msg) {
+  static std::atomic<uint32_t> launch_counter{1};
   DecodePlan pl;
   pa_status st = check_decode_args(a, true, msg);
   if (st != PA_OK) return st;
-  st = plan_decode(a, device_sm_count(), pl, msg);
+  const int sms = device_sm_count();
+  st = plan_decode(a, sms, pl, msg);
   if (st != PA_OK) return st;
-  if (pl.workspace > 0) {
-    if (a.workspace == nullptr || a.workspace_bytes < pl.workspace) {
-      msg = "workspace smaller than pa_decode_workspace_size()";
-      return PA_EINVAL;
-    }
-    if (!aligned(a.workspace, 256)) {
-      msg = "workspace must be 256-byte aligned";
-      return PA_EINVAL;
-    }
+  if (a.workspace == nullptr || a.workspace_bytes < pl.workspace) {
+    msg = "workspace smaller than pa_decode_workspace_size()";
+    return PA_EINVAL;
+  }
+  if (!aligned(a.workspace, 256)) {
+    msg = "workspace must be 256-byte aligned";
+    return PA_EINVAL;
   }
   if (a.num_seqs == 0) return PA_OK;
 
@@ -227,17 +258,11 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
   if (st != PA_OK) return st;
 
   DecodeParams p{};
-  p.q = a.q;
-  p.out = a.out;
-  p.block_tables = a.block_tables;
-  p.ctx_lens = a.ctx_lens;
-  const size_t slots = static_cast<size_t>(a.num_seqs) * a.num_q_heads * pl.max_splits;
-  p.part_o = pl.workspace ? static_cast<float*>(a.workspace) : nullptr;
-  p.part_ml = pl.workspace ? reinterpret_cast<float2*>(static_cast<char*>(a.workspace) +
-                                                       ((slots * a.head_dim * 4 + 255) / 256) * 256)
-                           : nullptr;
+  char* ws = static_cast<char*>(a.workspace);
+  p.counters = reinterpret_cast<unsigned long long*>(ws);
+  p.part_o = pl.max_splits > 1 ? reinterpret_cast<float*>(ws + 256) : nullptr;
+  p.part_ml = pl.max_splits > 1 ? reinterpret_cast<float2*>(ws + 256 + pl.partial_o_bytes) : nullptr;
   p.err = a.err_flag;
-  p.num_seqs = a.num_seqs;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
@@ -250,32 +275,52 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
   p.stages = pl.stages;
   p.region_stride = pl.region_stride;
   p.stage_bytes = pl.stage_bytes;
-  p.ctl_offset = pl.ctl_offset;
+  p.off_merge = pl.off_merge;
+  p.off_q = pl.off_q;
+  p.off_bar = pl.off_bar;
+  p.off_meta = pl.off_meta;
+  p.off_items = pl.off_items;
+  p.off_tbl = pl.off_tbl;
+  p.tbl_stride = pl.tbl_stride;
+  p.off_scan = pl.off_scan;
   p.score_scale = a.scale * a.k_scale * kLog2e;
   p.v_scale = a.v_scale;
   p.q_bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
 
   const int group = a.num_q_heads / a.num_kv_heads;
-  dim3 grid(pl.max_splits, a.num_kv_heads, a.num_seqs);
-  cudaError_t e;
-  switch (a.kv_dtype) {
-    case PA_F16:
-      e = launch_decode_f16(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
-      break;
-    case PA_BF16:
-      e = launch_decode_bf16(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
-      break;
-    default:
-      e = launch_decode_e4m3(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
-      break;
+  const int elt_q = 2;
+  const dim3 grid(std::max(1, sms));
+  for (int s0 = 0; s0 < a.num_seqs; s0 += pl.seqs_per_launch) {
+    const int n = std::min(pl.seqs_per_launch, a.num_seqs - s0);
+    const size_t row = static_cast<size_t>(s0) * a.num_q_heads * a.head_dim * elt_q;
+    p.q = static_cast<const char*>(a.q) + row;
+    p.out = static_cast<char*>(a.out) + row;
+    p.block_tables = a.block_tables + static_cast<size_t>(s0) * a.max_blocks_per_seq;
+    p.ctx_lens = a.ctx_lens + s0;
+    p.num_seqs = n;
+    p.launch_id = launch_counter.fetch_add(1);
+    if (p.launch_id == 0) p.launch_id = launch_counter.fetch_add(1);
+    cudaError_t e;
+    switch (a.kv_dtype) {
+      case PA_F16:
+        e = launch_decode_f16(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
+        break;
+      case PA_BF16:
+        e = launch_decode_bf16(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
+        break;
+      default:
+        e = launch_decode_e4m3(a.head_dim, group, kmap, vmap, p, grid, pl.smem_bytes, stream);
+        break;
+    }
+    st = cuda_status(e, "pa_decode kernel launch", msg);
+    if (st != PA_OK) return st;
+    if (pl.max_splits > 1) {
+      e = launch_reduce(a.head_dim, p, a.q_dtype == PA_BF16, stream);
+      st = cuda_status(e, "pa_decode reduce launch", msg);
+      if (st != PA_OK) return st;
+    }
   }
-  st = cuda_status(e, "pa_decode kernel launch", msg);
-  if (st != PA_OK) return st;
-  if (pl.max_splits > 1) {
-    e = launch_reduce(a.head_dim, p, a.q_dtype == PA_BF16, stream);
-    st = cuda_status(e, "pa_decode reduce launch", msg);
-  }
-  return st;
+  return PA_OK;
 }
 
 cudaError_t launch_reduce(int head_dim, const DecodeParams& p, bool out_bf16, cudaStream_t stream) {

@@ -214,3 +214,51 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 }  // namespace pa
+
+namespace pa {
+
+// 1-D bulk copy global -> shared completing on an mbarrier (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Named barrier 1 over `threads` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool bar_or(int threads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Ticket from a 64-bit counter tagged with a launch id in its high half. A word that does not
+// carry this launch's id (garbage, or left by an earlier launch) is re-armed to (id, 1) and the
+// thread that re-arms it takes ticket 0, so the counter needs no clearing before a launch.
+__device__ __forceinline__ uint32_t fetch_ticket(unsigned long long* ctr, uint32_t id) {
+  const unsigned long long tag = static_cast<unsigned long long>(id) << 32;
+  for (;;) {
+    const unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    if ((cur >> 32) == id) {
+      const unsigned long long old = atomicAdd(ctr, 1ull);
+      if ((old >> 32) == id) return static_cast<uint32_t>(old);
+    } else if (atomicCAS(ctr, cur, tag | 1ull) == cur) {
+      return 0u;
+    }
+  }
+}
+
+}  // namespace pa

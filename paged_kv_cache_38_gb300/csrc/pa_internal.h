@@ -16,17 +16,20 @@ struct DecodeParams;
 
 // Sizes of one pa_decode launch, derived only from the arguments and the SM count.
 struct DecodePlan {
-  int elt = 2;            // bytes per KV element
-  int regions = 1;        // 128-byte column regions per token row
-  int stage_tokens = 16;  // tokens per pipeline stage (max(16, block_size))
-  int region_stride = 0;  // bytes of one region of one block inside a stage
-  int stage_bytes = 0;    // bytes of K (or V) per stage
-  int stages = 0;         // ring depth
-  int split_tokens = 0;   // tokens per context split
+  int elt = 2;             // bytes per KV element
+  int regions = 1;         // 128-byte column regions per token row
+  int stage_tokens = 16;   // tokens per pipeline stage (max(16, block_size))
+  int region_stride = 0;   // bytes of one region of one block inside a stage
+  int stage_bytes = 0;     // bytes of K (or V) per stage
+  int stages = 0;          // ring depth
+  int split_tokens = 0;    // tokens per work item
   int max_splits = 1;
-  int ctl_offset = 0;     // start of barriers / table inside the aligned shared memory
-  size_t smem_bytes = 0;  // dynamic shared memory per CTA
-  size_t workspace = 0;   // bytes of split partials (0 when max_splits == 1)
+  int seqs_per_launch = 0; // sequences handled by one kernel launch
+  int off_merge = 0, off_q = 0, off_bar = 0, off_meta = 0, off_items = 0, off_tbl = 0, off_scan = 0;
+  int tbl_stride = 0;      // block-table entries per queued work item
+  size_t smem_bytes = 0;   // dynamic shared memory per CTA
+  size_t workspace = 0;    // bytes: 256 of work counters, then the split partials
+  size_t partial_o_bytes = 0;
 };
 
 // Validate decode arguments (no device access; pointers only when check_pointers). On failure
