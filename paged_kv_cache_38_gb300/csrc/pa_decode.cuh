@@ -29,6 +29,10 @@
 //     pa_reduce_kernel combines.
 #pragma once
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "pa_device.cuh"
 
 namespace pa {
@@ -682,7 +686,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // Several issuing warps keep enough copies in flight: one warp alone streams far below
     // the per-SM share of HBM bandwidth.
     const int pw = warp - 1;
-    const uint64_t pol = policy_evict_normal();
+    // K/V tiles are streamed once (shared-prompt blocks are re-read within microseconds by the
+    // neighbouring items of the other group members), so they are marked evict-first in L2.
+    const uint64_t pol = policy_evict_first();
     if (lane == 0 && pw == 0) {
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
@@ -868,6 +874,8 @@ template <int D>
 __global__ void __launch_bounds__(128) pa_reduce_kernel(const __grid_constant__ DecodeParams p,
                                                         int out_bf16) {
   constexpr int kPer = D / 32;
+  // Launched as a programmatic dependent of the decode kernel: wait until its results are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (gw >= p.num_seqs * p.num_q_heads) return;
@@ -915,6 +923,24 @@ __global__ void __launch_bounds__(128) pa_reduce_kernel(const __grid_constant__ 
 
 namespace pa {
 
+// Host: record of (kernel, device) pairs already opted in to the full shared memory.
+inline std::mutex& opt_in_mutex() {
+  static std::mutex m;
+  return m;
+}
+inline std::set<std::pair<const void*, int>>& opt_in_set() {
+  static std::set<std::pair<const void*, int>> s;
+  return s;
+}
+inline bool smem_opted_in(const void* fn, int dev) {
+  std::lock_guard<std::mutex> g(opt_in_mutex());
+  return opt_in_set().count({fn, dev}) != 0;
+}
+inline void mark_smem_opted_in(const void* fn, int dev) {
+  std::lock_guard<std::mutex> g(opt_in_mutex());
+  opt_in_set().insert({fn, dev});
+}
+
 // Host: launch the decode kernel instantiation for (KV, head_dim, group).
 template <int KV>
 cudaError_t launch_decode_kv(int head_dim, int group, const CUtensorMap& kmap,
@@ -937,9 +963,16 @@ cudaError_t launch_decode_kv(int head_dim, int group, const CUtensorMap& kmap,
   }
 #undef PA_DECODE_CASE
   if (fn == nullptr) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  // Opt in to the full shared memory once per device (not per call, so that launches can be
+  // captured into CUDA graphs without extra API calls).
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (!smem_opted_in(reinterpret_cast<const void*>(fn), dev)) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    mark_smem_opted_in(reinterpret_cast<const void*>(fn), dev);
+  }
   fn<<<grid, kDecodeThreads, smem, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }

@@ -325,12 +325,21 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
 
 cudaError_t launch_reduce(int head_dim, const DecodeParams& p, bool out_bf16, cudaStream_t stream) {
   const int warps = p.num_seqs * p.num_q_heads;
-  dim3 grid((warps + 3) / 4);
-  if (head_dim == 128)
-    pa_reduce_kernel<128><<<grid, 128, 0, stream>>>(p, out_bf16 ? 1 : 0);
-  else
-    pa_reduce_kernel<64><<<grid, 128, 0, stream>>>(p, out_bf16 ? 1 : 0);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the reduce grid is scheduled while the decode kernel drains
+  // and waits (griddepcontrol.wait) for its memory before reading the partials.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 3) / 4);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int flag = out_bf16 ? 1 : 0;
+  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<128>, p, flag);
+  return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<64>, p, flag);
 }
 
 }  // namespace pa
