@@ -25,8 +25,9 @@
 //     each 16-token tile a small dense contraction, done with mma.sync m16n8k16
 //     (S^T = K Q^T with the G query heads as the N dimension, then O^T += V^T P^T).
 //   * At the end of an item the consumer states are merged in shared memory; an item that covers
-//     its sequence's whole context writes the output, otherwise fp32 partials that
-//     pa_reduce_kernel combines.
+//     its sequence's whole context writes the output, otherwise fp32 partials (split-K, flash-
+//     decoding style) that pa_reduce_kernel combines. (Merging inside this kernel was measured
+//     slower: the GPU-scope fence each split needs stalls the consumers at every item.)
 #pragma once
 
 #include <mutex>
@@ -868,55 +869,64 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 }
 
-// Combine the split partials of every (sequence, query head) that used more than one split.
-// One warp per (sequence, head); lanes own head_dim/32 consecutive outputs.
+// Split-K combine: one CTA per (sequence, kv head) with more than one split. The (max, sum) pairs
+// of all splits of the group's heads are staged in shared memory and turned into weights
+// w_i = 2^(m_i - m*) / sum_j 2^(m_j - m*) l_j once per head; every output is then a weighted sum
+// of independent float4 loads of the split accumulators.
 template <int D>
 __global__ void __launch_bounds__(128) pa_reduce_kernel(const __grid_constant__ DecodeParams p,
-                                                        int out_bf16) {
-  constexpr int kPer = D / 32;
-  // Launched as a programmatic dependent of the decode kernel: wait until its results are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (gw >= p.num_seqs * p.num_q_heads) return;
-  const int seq = gw / p.num_q_heads;
+                                                        int group, int out_bf16) {
+  extern __shared__ float wts[];  // [group][nsplit][2]
+  const int unit = blockIdx.x;
+  const int seq = unit / p.num_kv_heads, kvh = unit % p.num_kv_heads;
   const int L = __ldg(p.ctx_lens + seq);
   if (L <= 0 || L > p.max_ctx || L > p.max_blocks * p.block_size) return;
-  const int nsplit = (L + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit <= 1) return;
-  const size_t slot0 = static_cast<size_t>(gw) * p.max_splits;
-
-  float mstar = -INFINITY;
-  for (int i = lane; i < nsplit; i += 32) mstar = fmaxf(mstar, p.part_ml[slot0 + i].x);
-  for (int off = 16; off; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-
-  float acc[kPer];
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  float den = 0.f;
-  if (mstar != -INFINITY) {
-    for (int i = 0; i < nsplit; ++i) {
-      const float2 ml = p.part_ml[slot0 + i];
-      const float wgt = ex2(ml.x - mstar);
-      den = fmaf(wgt, ml.y, den);
-      const float* src = p.part_o + (slot0 + i) * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(src);
-        acc[0] = fmaf(wgt, v.x, acc[0]);
-        acc[1] = fmaf(wgt, v.y, acc[1]);
-        acc[2] = fmaf(wgt, v.z, acc[2]);
-        acc[3] = fmaf(wgt, v.w, acc[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(src);
-        acc[0] = fmaf(wgt, v.x, acc[0]);
-        acc[1] = fmaf(wgt, v.y, acc[1]);
-      }
-    }
+  const int ns = (L + p.split_tokens - 1) / p.split_tokens;
+  if (ns <= 1) return;
+  const size_t head0 = static_cast<size_t>(seq) * p.num_q_heads + static_cast<size_t>(kvh) * group;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < group * ns; i += blockDim.x) {
+    const float2 ml = p.part_ml[(head0 + i / ns) * p.max_splits + i % ns];
+    wts[2 * i] = ml.x;
+    wts[2 * i + 1] = ml.y;
   }
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-#pragma unroll
-  for (int e = 0; e < kPer; ++e)
-    store_out(p.out, static_cast<size_t>(gw) * D + lane * kPer + e, acc[e] * inv, out_bf16 != 0);
+  __syncthreads();
+  if (tid < group) {
+    float* w = wts + 2 * tid * ns;
+    float mstar = -INFINITY;
+    for (int i = 0; i < ns; ++i) mstar = fmaxf(mstar, w[2 * i]);
+    float den = 0.f;
+    for (int i = 0; i < ns; ++i) {
+      const float e = mstar == -INFINITY ? 0.f : ex2(w[2 * i] - mstar);
+      den = fmaf(e, w[2 * i + 1], den);
+      w[2 * i] = e;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int i = 0; i < ns; ++i) w[2 * i] *= inv;
+  }
+  __syncthreads();
+  constexpr int kVec = D / 4;
+  for (int idx = tid; idx < group * kVec; idx += blockDim.x) {
+    const int n = idx / kVec, c = idx % kVec;
+    const float* w = wts + 2 * n * ns;
+    const float4* src =
+        reinterpret_cast<const float4*>(p.part_o + (head0 + n) * p.max_splits * D) + c;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int i = 0; i < ns; ++i) {
+      const float4 v = src[static_cast<size_t>(i) * kVec];
+      const float wi = w[2 * i];
+      acc.x = fmaf(wi, v.x, acc.x);
+      acc.y = fmaf(wi, v.y, acc.y);
+      acc.z = fmaf(wi, v.z, acc.z);
+      acc.w = fmaf(wi, v.w, acc.w);
+    }
+    const size_t o = (head0 + n) * D + 4 * c;
+    store_out(p.out, o, acc.x, out_bf16 != 0);
+    store_out(p.out, o + 1, acc.y, out_bf16 != 0);
+    store_out(p.out, o + 2, acc.z, out_bf16 != 0);
+    store_out(p.out, o + 3, acc.w, out_bf16 != 0);
+  }
 }
 
 }  // namespace pa

@@ -230,6 +230,10 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   const size_t slots = static_cast<size_t>(pl.seqs_per_launch) * a.num_q_heads * pl.max_splits;
   pl.partial_o_bytes = pl.max_splits > 1 ? up(slots * D * 4, 256) : 0;
   pl.workspace = 256 + (pl.max_splits > 1 ? pl.partial_o_bytes + slots * 8 : 0);
+  if (pl.max_splits > 1 && static_cast<size_t>(group) * pl.max_splits * 8 > 48 * 1024) {
+    msg = "too many context splits for the split-K combine; raise split_tokens";
+    return PA_EINVAL;
+  }
   return PA_OK;
 }
 
@@ -260,8 +264,9 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
   DecodeParams p{};
   char* ws = static_cast<char*>(a.workspace);
   p.counters = reinterpret_cast<unsigned long long*>(ws);
-  p.part_o = pl.max_splits > 1 ? reinterpret_cast<float*>(ws + 256) : nullptr;
-  p.part_ml = pl.max_splits > 1 ? reinterpret_cast<float2*>(ws + 256 + pl.partial_o_bytes) : nullptr;
+  char* parts = ws + 256;
+  p.part_o = pl.max_splits > 1 ? reinterpret_cast<float*>(parts) : nullptr;
+  p.part_ml = pl.max_splits > 1 ? reinterpret_cast<float2*>(parts + pl.partial_o_bytes) : nullptr;
   p.err = a.err_flag;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
@@ -315,31 +320,24 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
     st = cuda_status(e, "pa_decode kernel launch", msg);
     if (st != PA_OK) return st;
     if (pl.max_splits > 1) {
-      e = launch_reduce(a.head_dim, p, a.q_dtype == PA_BF16, stream);
-      st = cuda_status(e, "pa_decode reduce launch", msg);
+      e = launch_reduce(a.head_dim, group, pl.max_splits, p, a.q_dtype == PA_BF16, stream);
+      st = cuda_status(e, "pa_decode split-K combine launch", msg);
       if (st != PA_OK) return st;
     }
   }
   return PA_OK;
 }
 
-cudaError_t launch_reduce(int head_dim, const DecodeParams& p, bool out_bf16, cudaStream_t stream) {
-  const int warps = p.num_seqs * p.num_q_heads;
-  // Programmatic dependent launch: the reduce grid is scheduled while the decode kernel drains
-  // and waits (griddepcontrol.wait) for its memory before reading the partials.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((warps + 3) / 4);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+cudaError_t launch_reduce(int head_dim, int group, int max_splits, const DecodeParams& p,
+                          bool out_bf16, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(p.num_seqs) * p.num_kv_heads);
+  const size_t smem = static_cast<size_t>(group) * max_splits * 8;
   const int flag = out_bf16 ? 1 : 0;
-  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<128>, p, flag);
-  return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<64>, p, flag);
+  if (head_dim == 128)
+    pa_reduce_kernel<128><<<grid, 128, smem, stream>>>(p, group, flag);
+  else
+    pa_reduce_kernel<64><<<grid, 128, smem, stream>>>(p, group, flag);
+  return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -262,3 +262,4 @@ __device__ __forceinline__ uint32_t fetch_ticket(unsigned long long* ctr, uint32
 }
 
 }  // namespace pa
+

@@ -48,7 +48,9 @@ cudaError_t launch_decode_bf16(int head_dim, int group, const CUtensorMap& kmap,
 cudaError_t launch_decode_e4m3(int head_dim, int group, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, const DecodeParams& p, dim3 grid,
                                size_t smem, cudaStream_t stream);
-cudaError_t launch_reduce(int head_dim, const DecodeParams& p, bool out_bf16, cudaStream_t stream);
+
+cudaError_t launch_reduce(int head_dim, int group, int max_splits, const DecodeParams& p,
+                          bool out_bf16, cudaStream_t stream);
 
 pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& msg);
 

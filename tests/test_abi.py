@@ -74,6 +74,7 @@ def _args(**kw):
 def test_workspace_size_and_validation_on_host():
     lib = pa.lib()
     assert pa.pa_decode_workspace_size(_args()) > 0
+    # the work counters only, no split partials
     assert pa.pa_decode_workspace_size(_args(max_ctx_len=16, split_tokens=16)) == 256
     for bad in (dict(head_dim=96), dict(block_size=12), dict(num_q_heads=30),
                 dict(max_ctx_len=5000), dict(split_tokens=24)):
