@@ -201,6 +201,28 @@ pa_status pa_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t num
                          size_t block_bytes, pa_swap_dir dir, void* staging, size_t staging_bytes,
                          pa_stream stream);
 
+/*
+ * pa_decode_static_workspace - pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a convenience of this library. Some callers cannot call
+ * cudaMalloc or any allocator -- an inference runtime whose device memory is one arena planned
+ * ahead of time, a plugin that is handed only the tensors it works on, a latency-critical path
+ * where an allocation could block. This call takes the same arguments as pa_decode but ignores
+ * args->workspace and args->workspace_bytes: the split-K partials and work counters live in a
+ * scratch array of PA_STATIC_WORKSPACE_BYTES inside the library's own device memory. That array
+ * exists on every GPU that loads the library, from load until the process exits.
+ *   - It allocates nothing. A decode whose pa_decode_workspace_size() exceeds
+ *     PA_STATIC_WORKSPACE_BYTES is rejected with PA_EINVAL (raise split_tokens, or use
+ *     pa_decode with a workspace of your own).
+ *   - The first call on a device looks up the array's device address (once per device); make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps whatever the last call left in
+ *     it (the kernel needs no zeroed scratch). Calls that may overlap on the GPU -- on different
+ *     streams, or from different host threads -- race on it and must be serialised by the caller.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+pa_status pa_decode_static_workspace(const pa_decode_args* args, pa_stream stream);
+
 /* Static description of a status code. */
 const char* pa_status_string(pa_status status);
 

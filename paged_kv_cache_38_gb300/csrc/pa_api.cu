@@ -17,6 +17,10 @@ pa_status finish(pa_status st, const std::string& msg) {
 
 }  // namespace
 
+namespace pa {
+pa_status record_error(pa_status st, const std::string& msg) { return finish(st, msg); }
+}  // namespace pa
+
 extern "C" {
 
 const char* pa_status_string(pa_status status) {

@@ -68,6 +68,9 @@ pa_status run_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t nu
                           size_t block_bytes, pa_swap_dir dir, void* staging, size_t staging_bytes,
                           cudaStream_t stream, std::string& msg);
 
+// Records msg as the calling thread's last-error message and returns st.
+pa_status record_error(pa_status st, const std::string& msg);
+
 // Sets msg from a CUDA error and returns PA_ECUDA (or PA_OK for cudaSuccess).
 pa_status cuda_status(cudaError_t e, const char* what, std::string& msg);
 

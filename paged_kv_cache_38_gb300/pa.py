@@ -19,6 +19,7 @@ PA_OK, PA_EINVAL, PA_EUNSUPPORTED, PA_ECUDA = 0, 1, 2, 3
 PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 PA_SWAP_OUT, PA_SWAP_IN = 0, 1
 PA_ERR_BLOCK_ID, PA_ERR_CTX_LEN, PA_ERR_TIMEOUT = 1, 2, 4
+PA_STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -71,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.pa_swap_blocks.restype = ctypes.c_int
         L.pa_swap_blocks.argtypes = [_vp, _vp, _i32, _vp, _vp, _i32, _i32, ctypes.c_size_t,
                                      ctypes.c_int, _vp, ctypes.c_size_t, _vp]
+        L.pa_decode_static_workspace.restype = ctypes.c_int
+        L.pa_decode_static_workspace.argtypes = [ctypes.POINTER(pa_decode_args), _vp]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_status_string.argtypes = [ctypes.c_int]
         L.pa_last_error_message.restype = ctypes.c_char_p
@@ -160,6 +163,24 @@ def pa_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
             args.workspace, args.workspace_bytes = workspace.data_ptr(), need
     _check(lib().pa_decode(ctypes.byref(args), _stream(stream)))
+    return out
+
+
+def pa_decode_static_workspace(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                               block_tables: torch.Tensor, ctx_lens: torch.Tensor, scale: float,
+                               *, out: Optional[torch.Tensor] = None, k_scale: float = 1.0,
+                               v_scale: float = 1.0, max_ctx_len: Optional[int] = None,
+                               split_tokens: int = 0, err_flag: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """pa_decode using the library's built-in scratch instead of a caller workspace, for callers
+    that must not allocate device memory. ``out`` should be passed in by such callers; it is
+    created here only for convenience when omitted."""
+    if out is None:
+        out = torch.empty_like(q)
+    args = make_decode_args(q, k_pool, v_pool, block_tables, ctx_lens, out, scale=scale,
+                            k_scale=k_scale, v_scale=v_scale, max_ctx_len=max_ctx_len,
+                            split_tokens=split_tokens, err_flag=err_flag)
+    _check(lib().pa_decode_static_workspace(ctypes.byref(args), _stream(stream)))
     return out
 
 
