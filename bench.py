@@ -3,7 +3,7 @@
 One step = one decode step of the shared-prompt GQA workload ("gqa_pressure": 100 sequences,
 32 query / 8 KV heads x 128, bf16, 16-token blocks, contexts U[256, 4096] raised to >= 513,
 25 groups of 4 sharing a 512-token prompt): pa_write_kv of the 100 new tokens, pa_copy_blocks of
-the 25 copy-on-write blocks, pa_decode (main kernel + split-K reduce), one layer. Inputs are
+the 25 copy-on-write blocks, pa_decode (one kernel incl. the split-K combine), one layer. Inputs are
 resident in HBM and larger than L2; L2 is also flushed between timed steps (outside the events).
 
 The metric is achieved HBM bandwidth: algorithmic bytes of the step (every distinct KV byte the
@@ -44,9 +44,9 @@ DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh", "pa_decode_host.cu", "pa_dec
 
 
 def split_tokens_for(spec: synth.DecodeSpec) -> int:
-    """Context split used by the benchmark (and by the full-size parity tests): ~256 KiB of K+V."""
+    """Context split used by the benchmark (and by the full-size parity tests): ~512 KiB of K+V."""
     elt = synth.ELT_BYTES[spec.kv_dtype]
-    return (256 * 1024) // (2 * spec.head_dim * elt)
+    return (512 * 1024) // (2 * spec.head_dim * elt)
 
 
 # ---------------------------------------------------------------------------- byte accounting
@@ -241,7 +241,7 @@ class Step:
         need = pa.pa_decode_workspace_size(args)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=case.q.device)
         self.max_splits = (self.max_ctx + split_tokens - 1) // split_tokens
-        self.launches = 3 + (1 if self.max_splits > 1 else 0)
+        self.launches = 3  # write-KV, copy-on-write, decode (split-K combine is in-kernel)
 
     def decode(self, q=None, block_tables=None, ctx_lens=None, out=None):
         c = self.case
@@ -332,7 +332,7 @@ def run_ours(args, world, rank, local) -> None:
     ms_per_step = total_ms / args.steps
     eager_ms = statistics.mean(time_steps(step.run, args.steps, flush))
 
-    # ---- the decode call alone (main kernel + split-K reduce), same stream, L2 flushed
+    # ---- the decode call alone (one kernel launch), same stream, L2 flushed
     dtimes = time_steps(decode_graph.replay, max(args.steps, 10), flush)
     dec_ms = statistics.mean(dtimes)
 
@@ -366,7 +366,7 @@ def run_ours(args, world, rank, local) -> None:
                          f"{spec.shared_prompt + 1}), {spec.num_seqs // spec.group_size} groups x "
                          f"{spec.group_size} share a {spec.shared_prompt}-token prompt, "
                          f"{case.cow_pairs.shape[0]} CoW copies/step, 1 layer"),
-            "step": "pa_write_kv + pa_copy_blocks + pa_decode (main + split-K reduce), "
+            "step": "pa_write_kv + pa_copy_blocks + pa_decode (split-K combine in-kernel), "
                     "replayed from a CUDA graph",
             "split_tokens": split, "num_blocks": case.num_blocks,
             "ctx_tokens": int(case.ctx_lens.sum()), "l2": "flushed between steps (untimed); "
@@ -376,7 +376,7 @@ def run_ours(args, world, rank, local) -> None:
         "decode_tokens_per_s": round(world * spec.num_seqs / (ms_per_step * 1e-3), 1),
         "ms_per_step_eager": round(eager_ms, 4),
         "bytes_per_step": {**dbytes, **mbytes, "total": step_bytes},
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (main + split-K reduce)",
+        "roofline": {"bound": "hbm", "kernel": "pa_decode_kernel",
                      "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,

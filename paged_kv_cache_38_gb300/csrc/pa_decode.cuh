@@ -26,8 +26,10 @@
 //     (S^T = K Q^T with the G query heads as the N dimension, then O^T += V^T P^T).
 //   * At the end of an item the consumer states are merged in shared memory; an item that covers
 //     its sequence's whole context writes the output, otherwise fp32 partials (split-K, flash-
-//     decoding style) that pa_reduce_kernel combines. (Merging inside this kernel was measured
-//     slower: the GPU-scope fence each split needs stalls the consumers at every item.)
+//     decoding style). When every CTA has run out of items, one grid-wide barrier (cooperative
+//     launch) separates the item phase from the combine phase, in which every warp of the grid
+//     combines the partials of one (sequence, query head). (Publishing each split with its own
+//     GPU-scope fence was measured slower: it stalls the consumers at every item.)
 #pragma once
 
 #include <mutex>
@@ -57,7 +59,7 @@ struct DecodeParams {
   const int32_t* ctx_lens;
   float* part_o;        // [num_seqs][num_q_heads][max_splits][D] unnormalised, v_scale applied
   float2* part_ml;      // [num_seqs][num_q_heads][max_splits] (max score in log2 units, weight sum)
-  unsigned long long* counters;  // [0] next work item, [1] CTAs finished (launch-id tagged)
+  unsigned long long* counters;  // [0] next item, [1] CTAs finished, [2] grid barrier (id-tagged)
   uint32_t launch_id;
   int32_t* err;
   int num_seqs, num_q_heads, num_kv_heads;
@@ -67,6 +69,7 @@ struct DecodeParams {
   int stages;           // shared-memory ring depth, a multiple of kConsumerWarps
   int region_stride;    // bytes of one 128-byte-wide column region of one block in a stage
   int stage_bytes;      // bytes of K (or V) in one stage
+  int stage_tokens;     // tokens per stage: a multiple of 16, at most 4 blocks
   // byte offsets from the 1024-aligned shared-memory base
   int off_merge, off_q, off_bar, off_meta, off_items, off_tbl, off_scan;
   int tbl_stride;       // block-table entries per item slot
@@ -521,6 +524,57 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, bool b
     static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
+// Combine the split partials of one (sequence, query head) with one warp: the (max, sum) pairs of
+// up to 32 splits per pass sit in the lanes, the weights w_i = 2^(m_i - m*) / sum_j 2^(m_j - m*)
+// l_j are formed with shuffles, then out = sum_i w_i * acc_i with float4 loads (lane c owns
+// columns 4c..4c+3).
+template <int D>
+__device__ void combine_head(const DecodeParams& p, int seq, size_t head, int lane, bool out_bf16) {
+  const int L = __ldg(p.ctx_lens + seq);
+  if (L <= 0 || L > p.max_ctx || L > p.max_blocks * p.block_size) return;
+  const int ns = (L + p.split_tokens - 1) / p.split_tokens;
+  if (ns <= 1) return;
+  constexpr int kVec = D / 4;
+  const size_t slot0 = head * p.max_splits;
+  // max over all splits
+  float mstar = -INFINITY;
+  for (int i = lane; i < ns; i += 32) mstar = fmaxf(mstar, __ldcg(&p.part_ml[slot0 + i].x));
+  for (int off = 16; off; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  const float4* src = reinterpret_cast<const float4*>(p.part_o + slot0 * D);
+  for (int i0 = 0; i0 < ns; i0 += 32) {
+    const int cnt = min(32, ns - i0);
+    float e = 0.f, l = 0.f;
+    if (lane < cnt && mstar != -INFINITY) {
+      const float2 ml = __ldcg(&p.part_ml[slot0 + i0 + lane]);
+      e = ex2(ml.x - mstar);
+      l = ml.y;
+    }
+    den = fmaf(e, l, den);
+#pragma unroll 4
+    for (int j = 0; j < cnt; ++j) {
+      const float ej = __shfl_sync(0xffffffffu, e, j);
+      if (lane < kVec) {
+        const float4 v = __ldcg(src + static_cast<size_t>(i0 + j) * kVec + lane);
+        acc.x = fmaf(ej, v.x, acc.x);
+        acc.y = fmaf(ej, v.y, acc.y);
+        acc.z = fmaf(ej, v.z, acc.z);
+        acc.w = fmaf(ej, v.w, acc.w);
+      }
+    }
+  }
+  for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  if (lane < kVec) {
+    const size_t o = head * D + 4 * lane;
+    store_out(p.out, o, acc.x * inv, out_bf16);
+    store_out(p.out, o + 1, acc.y * inv, out_bf16);
+    store_out(p.out, o + 2, acc.z * inv, out_bf16);
+    store_out(p.out, o + 3, acc.w * inv, out_bf16);
+  }
+}
+
 __device__ __forceinline__ int phs_of(const int (&phs)[4], int b) {
   return b == 0 ? phs[0] : b == 1 ? phs[1] : b == 2 ? phs[2] : phs[3];
 }
@@ -556,7 +610,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.num_seqs, Hkv = p.num_kv_heads, B = p.block_size, S = p.split_tokens;
-  const int st_tokens = max(16, B);
+  const int st_tokens = p.stage_tokens;
 
   // ---- prologue: work items per sequence (kv heads x splits) and their prefix sums
   {
@@ -857,6 +911,40 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
   }
 
+  // ---- split-K combine. The kernel is a cooperative launch (every CTA resident), so after one
+  // grid-wide barrier all partials are in memory and the CTAs combine them: one warp per
+  // (sequence, query head) with more than one split. One fence per CTA instead of one per item.
+  __syncthreads();
+  if (p.max_splits > 1) {
+    if (tid == 0) {
+      __threadfence();  // this CTA's partials are visible to the whole GPU before it arrives
+      fetch_ticket(p.counters + 2, p.launch_id);
+      const unsigned long long* ctr = p.counters + 2;
+      const unsigned long long start = global_ns();
+      bool ok = true;
+      for (uint32_t i = 0;; ++i) {
+        const unsigned long long v = *reinterpret_cast<const volatile unsigned long long*>(ctr);
+        if ((v >> 32) == p.launch_id && static_cast<uint32_t>(v) >= gridDim.x) break;
+        if ((i & 63u) == 63u && global_ns() - start > kWaitLimitNs) {
+          ok = false;
+          break;
+        }
+      }
+      __threadfence();
+      if (!ok) {
+        flag_error(p.err, kErrTimeout);
+        *abort_flag = 1;
+      }
+    }
+    __syncthreads();
+    if (!*abort_flag) {
+      const int nwarps = kDecodeThreads / 32;
+      const int heads = N * p.num_q_heads;
+      for (int h = blockIdx.x * nwarps + warp; h < heads; h += gridDim.x * nwarps)
+        combine_head<D>(p, h / p.num_q_heads, static_cast<size_t>(h), lane, qbf);
+    }
+  }
+
   // ---- the last CTA to finish clears the work counters for the next launch
   __syncthreads();
   if (tid == 0) {
@@ -865,67 +953,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (done == gridDim.x - 1) {
       atomicExch(p.counters, 0ull);
       atomicExch(p.counters + 1, 0ull);
+      atomicExch(p.counters + 2, 0ull);
     }
-  }
-}
-
-// Split-K combine: one CTA per (sequence, kv head) with more than one split. The (max, sum) pairs
-// of all splits of the group's heads are staged in shared memory and turned into weights
-// w_i = 2^(m_i - m*) / sum_j 2^(m_j - m*) l_j once per head; every output is then a weighted sum
-// of independent float4 loads of the split accumulators.
-template <int D>
-__global__ void __launch_bounds__(128) pa_reduce_kernel(const __grid_constant__ DecodeParams p,
-                                                        int group, int out_bf16) {
-  extern __shared__ float wts[];  // [group][nsplit][2]
-  const int unit = blockIdx.x;
-  const int seq = unit / p.num_kv_heads, kvh = unit % p.num_kv_heads;
-  const int L = __ldg(p.ctx_lens + seq);
-  if (L <= 0 || L > p.max_ctx || L > p.max_blocks * p.block_size) return;
-  const int ns = (L + p.split_tokens - 1) / p.split_tokens;
-  if (ns <= 1) return;
-  const size_t head0 = static_cast<size_t>(seq) * p.num_q_heads + static_cast<size_t>(kvh) * group;
-  const int tid = threadIdx.x;
-  for (int i = tid; i < group * ns; i += blockDim.x) {
-    const float2 ml = p.part_ml[(head0 + i / ns) * p.max_splits + i % ns];
-    wts[2 * i] = ml.x;
-    wts[2 * i + 1] = ml.y;
-  }
-  __syncthreads();
-  if (tid < group) {
-    float* w = wts + 2 * tid * ns;
-    float mstar = -INFINITY;
-    for (int i = 0; i < ns; ++i) mstar = fmaxf(mstar, w[2 * i]);
-    float den = 0.f;
-    for (int i = 0; i < ns; ++i) {
-      const float e = mstar == -INFINITY ? 0.f : ex2(w[2 * i] - mstar);
-      den = fmaf(e, w[2 * i + 1], den);
-      w[2 * i] = e;
-    }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int i = 0; i < ns; ++i) w[2 * i] *= inv;
-  }
-  __syncthreads();
-  constexpr int kVec = D / 4;
-  for (int idx = tid; idx < group * kVec; idx += blockDim.x) {
-    const int n = idx / kVec, c = idx % kVec;
-    const float* w = wts + 2 * n * ns;
-    const float4* src =
-        reinterpret_cast<const float4*>(p.part_o + (head0 + n) * p.max_splits * D) + c;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int i = 0; i < ns; ++i) {
-      const float4 v = src[static_cast<size_t>(i) * kVec];
-      const float wi = w[2 * i];
-      acc.x = fmaf(wi, v.x, acc.x);
-      acc.y = fmaf(wi, v.y, acc.y);
-      acc.z = fmaf(wi, v.z, acc.z);
-      acc.w = fmaf(wi, v.w, acc.w);
-    }
-    const size_t o = (head0 + n) * D + 4 * c;
-    store_out(p.out, o, acc.x, out_bf16 != 0);
-    store_out(p.out, o + 1, acc.y, out_bf16 != 0);
-    store_out(p.out, o + 2, acc.z, out_bf16 != 0);
-    store_out(p.out, o + 3, acc.w, out_bf16 != 0);
   }
 }
 
@@ -983,8 +1012,18 @@ cudaError_t launch_decode_kv(int head_dim, int group, const CUtensorMap& kmap,
     if (e != cudaSuccess) return e;
     mark_smem_opted_in(reinterpret_cast<const void*>(fn), dev);
   }
-  fn<<<grid, kDecodeThreads, smem, stream>>>(kmap, vmap, p);
-  return cudaGetLastError();
+  // Cooperative launch: the combine phase waits on every CTA, so all must be resident at once.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, kmap, vmap, p);
 }
 
 }  // namespace pa

@@ -158,11 +158,13 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   const int group = a.num_q_heads / a.num_kv_heads;
   pl.elt = a.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
   pl.regions = D * pl.elt / 128;
-  pl.stage_tokens = std::max(16, B);
+  // 16 tokens per stage (32 for 1-byte KV, so a stage still moves 8 KiB per head pair of
+  // K and V and the per-stage costs are paid half as often), at most 4 blocks per stage.
+  pl.stage_tokens = std::max(B, std::min(pl.elt == 1 ? 32 : 16, 4 * B));
   pl.region_stride = std::max(B * 128, 1024);
   pl.stage_bytes = (pl.stage_tokens / B) * pl.regions * pl.region_stride;
 
-  const int stok = pl.stage_tokens;
+  const int stok = std::max(16, B);  // split granularity of the API
   if (a.split_tokens > 0) {
     if (a.split_tokens % stok != 0) {
       msg = "split_tokens must be a multiple of max(16, block_size)";
@@ -170,8 +172,8 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
     }
     pl.split_tokens = a.split_tokens;
   } else {
-    // work items of about 256 KiB of K+V, fewer tokens when there would be too few items
-    int tokens = (256 * 1024) / (2 * D * pl.elt);
+    // work items of about 512 KiB of K+V, fewer tokens when there would be too few items
+    int tokens = (512 * 1024) / (2 * D * pl.elt);
     const long long units = static_cast<long long>(a.num_seqs) * a.num_kv_heads;
     const int sms = sm_count > 0 ? sm_count : 148;
     while (tokens > 4 * stok && units * ((a.max_ctx_len + tokens - 1) / tokens) < 8LL * sms)
@@ -230,10 +232,6 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   const size_t slots = static_cast<size_t>(pl.seqs_per_launch) * a.num_q_heads * pl.max_splits;
   pl.partial_o_bytes = pl.max_splits > 1 ? up(slots * D * 4, 256) : 0;
   pl.workspace = 256 + (pl.max_splits > 1 ? pl.partial_o_bytes + slots * 8 : 0);
-  if (pl.max_splits > 1 && static_cast<size_t>(group) * pl.max_splits * 8 > 48 * 1024) {
-    msg = "too many context splits for the split-K combine; raise split_tokens";
-    return PA_EINVAL;
-  }
   return PA_OK;
 }
 
@@ -280,6 +278,7 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
   p.stages = pl.stages;
   p.region_stride = pl.region_stride;
   p.stage_bytes = pl.stage_bytes;
+  p.stage_tokens = pl.stage_tokens;
   p.off_merge = pl.off_merge;
   p.off_q = pl.off_q;
   p.off_bar = pl.off_bar;
@@ -319,25 +318,8 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
     }
     st = cuda_status(e, "pa_decode kernel launch", msg);
     if (st != PA_OK) return st;
-    if (pl.max_splits > 1) {
-      e = launch_reduce(a.head_dim, group, pl.max_splits, p, a.q_dtype == PA_BF16, stream);
-      st = cuda_status(e, "pa_decode split-K combine launch", msg);
-      if (st != PA_OK) return st;
-    }
   }
   return PA_OK;
-}
-
-cudaError_t launch_reduce(int head_dim, int group, int max_splits, const DecodeParams& p,
-                          bool out_bf16, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(p.num_seqs) * p.num_kv_heads);
-  const size_t smem = static_cast<size_t>(group) * max_splits * 8;
-  const int flag = out_bf16 ? 1 : 0;
-  if (head_dim == 128)
-    pa_reduce_kernel<128><<<grid, 128, smem, stream>>>(p, group, flag);
-  else
-    pa_reduce_kernel<64><<<grid, 128, smem, stream>>>(p, group, flag);
-  return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -18,7 +18,7 @@ struct DecodeParams;
 struct DecodePlan {
   int elt = 2;             // bytes per KV element
   int regions = 1;         // 128-byte column regions per token row
-  int stage_tokens = 16;   // tokens per pipeline stage (max(16, block_size))
+  int stage_tokens = 16;   // tokens per pipeline stage (16, or 32 for 1-byte KV; >= block_size)
   int region_stride = 0;   // bytes of one region of one block inside a stage
   int stage_bytes = 0;     // bytes of K (or V) per stage
   int stages = 0;          // ring depth
@@ -48,9 +48,6 @@ cudaError_t launch_decode_bf16(int head_dim, int group, const CUtensorMap& kmap,
 cudaError_t launch_decode_e4m3(int head_dim, int group, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, const DecodeParams& p, dim3 grid,
                                size_t smem, cudaStream_t stream);
-
-cudaError_t launch_reduce(int head_dim, int group, int max_splits, const DecodeParams& p,
-                          bool out_bf16, cudaStream_t stream);
 
 pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& msg);
 
