@@ -44,9 +44,9 @@ DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh", "pa_decode_host.cu", "pa_dec
 
 
 def split_tokens_for(spec: synth.DecodeSpec) -> int:
-    """Context split used by the benchmark (and by the full-size parity tests): ~512 KiB of K+V."""
-    elt = synth.ELT_BYTES[spec.kv_dtype]
-    return (512 * 1024) // (2 * spec.head_dim * elt)
+    """Context split used by the benchmark (and by the full-size parity tests): 512 tokens for
+    16-bit KV, 2048 for E4M3 (the library's own default for these shapes)."""
+    return 2048 if synth.ELT_BYTES[spec.kv_dtype] == 1 else 512
 
 
 # ---------------------------------------------------------------------------- byte accounting

@@ -524,34 +524,39 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, bool b
     static_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
-// Combine the split partials of one (sequence, query head) with one warp: the (max, sum) pairs of
-// up to 32 splits per pass sit in the lanes, the weights w_i = 2^(m_i - m*) / sum_j 2^(m_j - m*)
-// l_j are formed with shuffles, then out = sum_i w_i * acc_i with float4 loads (lane c owns
-// columns 4c..4c+3).
+// Combine the ns split partials of one (sequence, query head) with one warp: lane i holds the
+// (max, sum) pair of split i of each pass of 32, the weights w_i = 2^(m_i - m*) / sum_j
+// 2^(m_j - m*) l_j are formed with shuffles, then out = sum_i w_i * acc_i with float4 loads
+// (lane c owns columns 4c..4c+3). Two dependent memory rounds when ns <= 32.
 template <int D>
-__device__ void combine_head(const DecodeParams& p, int seq, size_t head, int lane, bool out_bf16) {
-  const int L = __ldg(p.ctx_lens + seq);
-  if (L <= 0 || L > p.max_ctx || L > p.max_blocks * p.block_size) return;
-  const int ns = (L + p.split_tokens - 1) / p.split_tokens;
-  if (ns <= 1) return;
+__device__ void combine_head(const DecodeParams& p, int ns, size_t head, int lane, bool out_bf16) {
   constexpr int kVec = D / 4;
   const size_t slot0 = head * p.max_splits;
-  // max over all splits
-  float mstar = -INFINITY;
-  for (int i = lane; i < ns; i += 32) mstar = fmaxf(mstar, __ldcg(&p.part_ml[slot0 + i].x));
+  float m_own = -INFINITY, l_own = 0.f;  // split `lane` (first pass of 32)
+  if (lane < ns) {
+    const float2 ml = __ldcg(&p.part_ml[slot0 + lane]);
+    m_own = ml.x;
+    l_own = ml.y;
+  }
+  float mstar = m_own;
+  for (int i = lane + 32; i < ns; i += 32) mstar = fmaxf(mstar, __ldcg(&p.part_ml[slot0 + i].x));
   for (int off = 16; off; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
   const float4* src = reinterpret_cast<const float4*>(p.part_o + slot0 * D);
   for (int i0 = 0; i0 < ns; i0 += 32) {
     const int cnt = min(32, ns - i0);
-    float e = 0.f, l = 0.f;
+    float e = 0.f;
     if (lane < cnt && mstar != -INFINITY) {
-      const float2 ml = __ldcg(&p.part_ml[slot0 + i0 + lane]);
-      e = ex2(ml.x - mstar);
-      l = ml.y;
+      float m = m_own, l = l_own;
+      if (i0 > 0) {
+        const float2 ml = __ldcg(&p.part_ml[slot0 + i0 + lane]);
+        m = ml.x;
+        l = ml.y;
+      }
+      e = ex2(m - mstar);
+      den = fmaf(e, l, den);
     }
-    den = fmaf(e, l, den);
 #pragma unroll 4
     for (int j = 0; j < cnt; ++j) {
       const float ej = __shfl_sync(0xffffffffu, e, j);
@@ -940,8 +945,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     if (!*abort_flag) {
       const int nwarps = kDecodeThreads / 32;
       const int heads = N * p.num_q_heads;
-      for (int h = blockIdx.x * nwarps + warp; h < heads; h += gridDim.x * nwarps)
-        combine_head<D>(p, h / p.num_q_heads, static_cast<size_t>(h), lane, qbf);
+      for (int h = blockIdx.x * nwarps + warp; h < heads; h += gridDim.x * nwarps) {
+        const int seq = h / p.num_q_heads;
+        const int ns = (prefix[seq + 1] - prefix[seq]) / Hkv;  // splits of this sequence (0: none)
+        if (ns > 1) combine_head<D>(p, ns, static_cast<size_t>(h), lane, qbf);
+      }
     }
   }
 

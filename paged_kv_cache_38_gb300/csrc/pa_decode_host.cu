@@ -172,8 +172,9 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
     }
     pl.split_tokens = a.split_tokens;
   } else {
-    // work items of about 512 KiB of K+V, fewer tokens when there would be too few items
-    int tokens = (512 * 1024) / (2 * D * pl.elt);
+    // 512-token work items for 16-bit KV, 2048 for 1-byte KV (its 32-token stages amortise the
+    // per-item merge over more stages); fewer tokens when there would be too few items
+    int tokens = pl.elt == 1 ? 2048 : 512;
     const long long units = static_cast<long long>(a.num_seqs) * a.num_kv_heads;
     const int sms = sm_count > 0 ? sm_count : 148;
     while (tokens > 4 * stok && units * ((a.max_ctx_len + tokens - 1) / tokens) < 8LL * sms)

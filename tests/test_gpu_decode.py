@@ -129,7 +129,10 @@ def test_full_size_sampled(name):
     if case.cow_pairs.numel():
         pa.pa_copy_blocks([case.k_pool], [case.v_pool], case.cow_pairs)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = gpu_decode(case, err_flag=err, max_ctx_len=int(case.ctx_lens.max()))
+    import bench
+
+    out = gpu_decode(case, err_flag=err, max_ctx_len=int(case.ctx_lens.max()),
+                     split_tokens=bench.split_tokens_for(spec))
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     rng = np.random.default_rng(7)
