@@ -49,7 +49,13 @@ constexpr int kMaxStages = 32;
 constexpr int kItemSlots = 4;          // work items queued ahead by the scheduler warp
 constexpr int kMaxItemBlocks = 256;    // block-table entries of one work item
 constexpr int kMaxSeqsPerLaunch = 4096;
-constexpr int kScanSlots = kDecodeThreads;
+constexpr int kScanWarps = kDecodeThreads / 32;
+constexpr int kRemBuckets = 32;  // size classes of the last-split items (longest first)
+// ints of the prologue's scan area for n sequences: two prefix arrays, the part-2 order, the
+// warp totals and the per-warp bucket counts
+__host__ __device__ constexpr size_t scan_ints(size_t n) {
+  return 3 * n + 2 + 2 * kScanWarps + kScanWarps * kRemBuckets + 2 * kRemBuckets;
+}
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeParams {
@@ -529,7 +535,7 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, bool b
 // 2^(m_j - m*) l_j are formed with shuffles, then out = sum_i w_i * acc_i with float4 loads
 // (lane c owns columns 4c..4c+3). Two dependent memory rounds when ns <= 32.
 template <int D>
-__device__ void combine_head(const DecodeParams& p, int ns, size_t head, int lane, bool out_bf16) {
+__device__ void combine_head_long(const DecodeParams& p, int ns, size_t head, int lane, bool out_bf16) {
   constexpr int kVec = D / 4;
   const size_t slot0 = head * p.max_splits;
   float m_own = -INFINITY, l_own = 0.f;  // split `lane` (first pass of 32)
@@ -580,6 +586,72 @@ __device__ void combine_head(const DecodeParams& p, int ns, size_t head, int lan
   }
 }
 
+// Combine of up to 32 splits: the (max, sum) pair of split `lane` and the first batch of
+// partial rows are loaded together, so one head costs about one L2 round trip. Lane l covers
+// float4 column l % (D / 4) of rows l / (D / 4), l / (D / 4) + 32 / (D / 4), ...
+template <int D>
+__device__ void combine_head(const DecodeParams& p, int ns, size_t head, int lane, bool out_bf16) {
+  constexpr int kVec = D / 4;
+  constexpr int kRows = 32 / kVec;
+  constexpr int kBatch = 8;
+  if (ns > 32) {
+    combine_head_long<D>(p, ns, head, lane, out_bf16);
+    return;
+  }
+  const size_t slot0 = head * p.max_splits;
+  const float4* src = reinterpret_cast<const float4*>(p.part_o + slot0 * D);
+  const int col = lane % kVec, row = lane / kVec;
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < ns) ml = __ldcg(&p.part_ml[slot0 + lane]);
+  float4 v[kBatch];
+#pragma unroll
+  for (int j = 0; j < kBatch; ++j) {
+    const int i = j * kRows + row;
+    v[j] = i < ns ? __ldcg(src + static_cast<size_t>(i) * kVec + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float mstar = ml.x;
+  for (int off = 16; off; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+  const float e = (lane < ns && mstar != -INFINITY) ? ex2(ml.x - mstar) : 0.f;
+  float den = e * ml.y;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i0 = 0; i0 < ns; i0 += kBatch * kRows) {
+    if (i0 > 0) {
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * kRows + row;
+        v[j] = i < ns ? __ldcg(src + static_cast<size_t>(i) * kVec + col)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int i = i0 + j * kRows + row;
+      const float ej = __shfl_sync(0xffffffffu, e, i & 31);
+      if (i < ns) {
+        acc.x = fmaf(ej, v[j].x, acc.x);
+        acc.y = fmaf(ej, v[j].y, acc.y);
+        acc.z = fmaf(ej, v[j].z, acc.z);
+        acc.w = fmaf(ej, v[j].w, acc.w);
+      }
+    }
+  }
+  if (kRows == 2) {
+    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 16);
+    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 16);
+    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 16);
+    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 16);
+  }
+  for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  if (lane < kVec) {
+    const size_t o = head * D + 4 * lane;
+    store_out(p.out, o, acc.x * inv, out_bf16);
+    store_out(p.out, o + 1, acc.y * inv, out_bf16);
+    store_out(p.out, o + 2, acc.z * inv, out_bf16);
+    store_out(p.out, o + 3, acc.w * inv, out_bf16);
+  }
+}
+
 __device__ __forceinline__ int phs_of(const int (&phs)[4], int b) {
   return b == 0 ? phs[0] : b == 1 ? phs[1] : b == 2 ? phs[2] : phs[3];
 }
@@ -610,31 +682,52 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   ItemDesc* items = reinterpret_cast<ItemDesc*>(bp + p.off_items);  // [kItemSlots]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(items + kItemSlots);
   int* tbl = reinterpret_cast<int*>(bp + p.off_tbl);      // [kItemSlots][tbl_stride]
-  int* prefix = reinterpret_cast<int*>(bp + p.off_scan);  // [num_seqs + 1]
-  int* partial = prefix + p.num_seqs + 1;                  // [kScanSlots]
+  int* pf1 = reinterpret_cast<int*>(bp + p.off_scan);  // [num_seqs + 1] full-split items
+  int* pf2 = pf1 + p.num_seqs + 1;                       // [num_seqs + 1] last-split items
+  int* order2 = pf2 + p.num_seqs + 1;                    // [num_seqs] part-2 sequence order
+  int* wsum = order2 + p.num_seqs;                       // [2 * kScanWarps] warp totals
+  int* wcnt = wsum + 2 * kScanWarps;                     // [kScanWarps][kRemBuckets]
+  int* bstart = wcnt + kScanWarps * kRemBuckets;         // [kRemBuckets] next free position
+  int* bcnt = bstart + kRemBuckets;                      // [kRemBuckets] sequences per bucket
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int N = p.num_seqs, Hkv = p.num_kv_heads, B = p.block_size, S = p.split_tokens;
   const int st_tokens = p.stage_tokens;
 
-  // ---- prologue: work items per sequence (kv heads x splits) and their prefix sums
+  // ---- prologue: the work list. Part 1 holds every full-length split of every sequence
+  // (sequence order, then kv head, then split); part 2 the shorter last split of each sequence
+  // whose context is not a multiple of split_tokens, longest first (a stable counting sort
+  // over kRemBuckets size classes), so the list ends with the smallest items and the CTAs run
+  // out of work at nearly the same time. pf1/pf2 are per-sequence prefix sums of item counts.
+  // Every CTA builds the same list.
+  auto rem_bucket = [&](int L) -> int {  // size class of the last split, -1 if it is full/empty
+    const bool bad = L < 0 || L > p.max_ctx || L > p.max_blocks * B;
+    const int r = (bad || L == 0) ? 0 : L % S;
+    return r == 0 ? -1 : kRemBuckets - 1 - static_cast<int>((static_cast<int64_t>(r - 1) * kRemBuckets) / S);
+  };
+  if (tid < kScanWarps * kRemBuckets) wcnt[tid] = 0;
+  if (tid < kRemBuckets) bcnt[tid] = 0;
+  __syncthreads();
   {
     const int per = (N + kDecodeThreads - 1) / kDecodeThreads;
     const int s0 = min(N, tid * per), s1 = min(N, s0 + per);
-    int local = 0;
+    int c1 = 0, c2 = 0;
     for (int s = s0; s < s1; ++s) {
       const int L = __ldg(p.ctx_lens + s);
       const bool bad = L < 0 || L > p.max_ctx || L > p.max_blocks * B;
-      const int cnt = (bad || L == 0) ? 0 : ((L + S - 1) / S) * Hkv;
-      prefix[s] = cnt;
-      local += cnt;
+      const int nfull = (bad || L == 0) ? 0 : L / S;
+      const int rem = (bad || L == 0) ? 0 : (L % S != 0);
+      pf1[s] = nfull * Hkv;
+      pf2[s] = rem * Hkv;
+      if (rem) atomicAdd(&bcnt[rem_bucket(L)], 1);
+      c1 += nfull * Hkv;
+      c2 += rem * Hkv;
       if ((bad || L == 0) && (s % gridDim.x) == blockIdx.x) {
         if (bad) flag_error(p.err, kErrCtxLen);
         const size_t row0 = static_cast<size_t>(s) * p.num_q_heads * D;
         for (int i = 0; i < p.num_q_heads * D; ++i) store_out(p.out, row0 + i, 0.f, qbf);
       }
     }
-    partial[tid] = local;
     if (tid == 0) {
       *abort_flag = 0;
       for (int s = 0; s < p.stages; ++s) {
@@ -647,26 +740,89 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       fence_barrier_init();
     }
-    __syncthreads();
-    if (tid == 0) {
-      int run = 0;
-      for (int i = 0; i < kDecodeThreads; ++i) {
-        const int c = partial[i];
-        partial[i] = run;
-        run += c;
+    // block-wide exclusive scan of (c1, c2): warp scans, then a scan of the warp totals
+    constexpr int kWarps = kDecodeThreads / 32;
+    int i1 = c1, i2 = c2;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t1 = __shfl_up_sync(0xffffffffu, i1, off);
+      const int t2 = __shfl_up_sync(0xffffffffu, i2, off);
+      if (lane >= off) {
+        i1 += t1;
+        i2 += t2;
       }
-      prefix[N] = run;
+    }
+    if (lane == 31) {
+      wsum[2 * warp] = i1;
+      wsum[2 * warp + 1] = i2;
     }
     __syncthreads();
-    int run = partial[tid];
+    if (warp == 0) {
+      const int v1 = lane < kWarps ? wsum[2 * lane] : 0;
+      const int v2 = lane < kWarps ? wsum[2 * lane + 1] : 0;
+      int u1 = v1, u2 = v2;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t1 = __shfl_up_sync(0xffffffffu, u1, off);
+        const int t2 = __shfl_up_sync(0xffffffffu, u2, off);
+        if (lane >= off) {
+          u1 += t1;
+          u2 += t2;
+        }
+      }
+      if (lane < kWarps) {
+        wsum[2 * lane] = u1 - v1;
+        wsum[2 * lane + 1] = u2 - v2;
+      }
+      if (lane == kWarps - 1) {
+        pf1[N] = u1;
+        pf2[N] = u2;
+      }
+    } else if (warp == 1) {  // bucket b (0 = longest) starts after the sequences of buckets < b
+      const int v = bcnt[lane];
+      int u = v;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, u, off);
+        if (lane >= off) u += t;
+      }
+      bstart[lane] = u - v;
+    }
+    __syncthreads();
+    int run1 = wsum[2 * warp] + i1 - c1, run2 = wsum[2 * warp + 1] + i2 - c2;
     for (int s = s0; s < s1; ++s) {
-      const int c = prefix[s];
-      prefix[s] = run;
-      run += c;
+      const int a1 = pf1[s], a2 = pf2[s];
+      pf1[s] = run1;
+      pf2[s] = run2;
+      run1 += a1;
+      run2 += a2;
     }
     __syncthreads();
   }
-  const int total_items = prefix[N];
+  // part 2 order: chunks of kDecodeThreads sequences; a sequence's position is its bucket's
+  // start, plus the bucket's sequences in earlier warps, plus those in earlier lanes
+  for (int c0 = 0; c0 < N; c0 += kDecodeThreads) {
+    const int s = c0 + tid;
+    const int b = s < N ? rem_bucket(__ldg(p.ctx_lens + s)) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, b);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (b >= 0 && rank == 0) wcnt[warp * kRemBuckets + b] = __popc(peers);
+    __syncthreads();
+    if (b >= 0) {
+      int pos = bstart[b] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w * kRemBuckets + b];
+      order2[pos] = s;
+    }
+    __syncthreads();
+    if (tid < kRemBuckets) {
+      int add = 0;
+      for (int w = 0; w < kScanWarps; ++w) {
+        add += wcnt[w * kRemBuckets + tid];
+        wcnt[w * kRemBuckets + tid] = 0;
+      }
+      bstart[tid] += add;
+    }
+    __syncthreads();
+  }
+  const int items1 = pf1[N];
+  const int total_items = items1 + pf2[N];
 
   if (warp == 0) {
     // ------------------------------------------------------------------ scheduler warp
@@ -686,13 +842,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       int item = 0, seq = 0;
       if (lane == 0) {
         item = static_cast<int>(fetch_ticket(p.counters, p.launch_id));
-        if (item < total_items) {
-          int lo = 0, hi = N - 1;  // largest s with prefix[s] <= item
+        if (item < items1) {
+          int lo = 0, hi = N - 1;  // largest s with pf1[s] <= item
           while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= item) lo = mid; else hi = mid - 1;
+            if (pf1[mid] <= item) lo = mid; else hi = mid - 1;
           }
           seq = lo;
+        } else if (item < total_items) {
+          seq = order2[(item - items1) / Hkv];
         }
       }
       item = __shfl_sync(0xffffffffu, item, 0);
@@ -706,9 +864,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         break;
       }
       const int L = __ldg(p.ctx_lens + seq);
-      const int nsplit = (L + S - 1) / S;
-      const int li = item - prefix[seq];
-      const int kvh = li / nsplit, split = li % nsplit;
+      const int nfull = (pf1[seq + 1] - pf1[seq]) / Hkv;
+      const int nsplit = nfull + (pf2[seq + 1] - pf2[seq]) / Hkv;
+      int kvh, split;
+      if (item < items1) {
+        const int li = item - pf1[seq];
+        kvh = li / nfull;
+        split = li % nfull;
+      } else {
+        kvh = (item - items1) % Hkv;
+        split = nfull;
+      }
       const int tok0 = split * S, tok_end = min(L, tok0 + S);
       const int blk0 = tok0 >> p.log2_block;
       const int nblk = ((tok_end - 1) >> p.log2_block) - blk0 + 1;
@@ -947,7 +1113,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       const int heads = N * p.num_q_heads;
       for (int h = blockIdx.x * nwarps + warp; h < heads; h += gridDim.x * nwarps) {
         const int seq = h / p.num_q_heads;
-        const int ns = (prefix[seq + 1] - prefix[seq]) / Hkv;  // splits of this sequence (0: none)
+        const int ns = (pf1[seq + 1] - pf1[seq] + pf2[seq + 1] - pf2[seq]) / Hkv;  // 0: none
         if (ns > 1) combine_head<D>(p, ns, static_cast<size_t>(h), lane, qbf);
       }
     }

@@ -199,7 +199,7 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   const size_t items = kItemSlots * sizeof(ItemDesc) + 16;
   pl.tbl_stride = ((tbl_entries + 3) / 4) * 4;
   const size_t tbls = static_cast<size_t>(kItemSlots) * pl.tbl_stride * 4;
-  const size_t scan = (static_cast<size_t>(pl.seqs_per_launch) + 1 + kScanSlots) * 4;
+  const size_t scan = scan_ints(static_cast<size_t>(pl.seqs_per_launch)) * 4;
   const size_t fixed = up(merge, 16) + up(qbytes, 128) + bars + meta + items + tbls + up(scan, 16);
   const size_t limit = 227 * 1024 - 1024;  // opt-in maximum per CTA, minus alignment slack
   if (fixed + 2 * static_cast<size_t>(pl.stage_bytes) * 8 > limit) {

@@ -63,6 +63,32 @@ def test_decode_edge_lengths():
             assert torch.count_nonzero(out[0]).item() == 0, "empty context must give zeros"
 
 
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_decode_split_counts(head_dim):
+    """Split counts on both sides of each combine batch boundary (8, 16, 32 partials per head)."""
+    lens = (16 * 8, 16 * 8 + 1, 16 * 16, 16 * 16 + 3, 16 * 17, 16 * 32, 16 * 32 + 1, 16 * 40 - 5)
+    spec = synth.DecodeSpec(f"splits_d{head_dim}", len(lens), 16, 4, head_dim, 16, "f16", "f16",
+                            ctx_lens=lens)
+    case = synth.make_case(spec, seed=head_dim).to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(case, split_tokens=16, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert max_abs_err(out, oracle_decode(case)) <= TOL["f16"]
+
+
+def test_decode_many_sequences():
+    """More sequences than one launch takes (4096) and than one scan chunk (416 threads), with
+    every remainder size class of the last split present."""
+    spec = synth.DecodeSpec("many", 4500, 4, 2, 64, 4, "f16", "f16", ctx_range=(0, 90))
+    case = synth.make_case(spec, seed=17).to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(case, split_tokens=32, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert max_abs_err(out, oracle_decode(case)) <= TOL["f16"]
+
+
 def test_decode_permutation_invariant_bitwise():
     """Moving blocks around the pool changes nothing, bit for bit (summary page, block table)."""
     spec = synth.SPECS["gqa_pressure"].scaled(num_seqs=16, ctx_range=(40, 500), shared_prompt=32)
