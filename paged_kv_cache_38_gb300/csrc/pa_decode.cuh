@@ -46,7 +46,7 @@ constexpr int kProducerWarps = 4;
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = 32 * (1 + kProducerWarps + kConsumerWarps);
 constexpr int kMaxStages = 32;
-constexpr int kItemSlots = 4;          // work items queued ahead by the scheduler warp
+constexpr int kItemSlots = 2;          // work items queued ahead by the scheduler warp
 constexpr int kMaxItemBlocks = 256;    // block-table entries of one work item
 constexpr int kMaxSeqsPerLaunch = 4096;
 constexpr int kScanWarps = kDecodeThreads / 32;
@@ -533,7 +533,7 @@ __device__ __forceinline__ void store_out(void* out, size_t idx, float v, bool b
 // Combine the ns split partials of one (sequence, query head) with one warp: lane i holds the
 // (max, sum) pair of split i of each pass of 32, the weights w_i = 2^(m_i - m*) / sum_j
 // 2^(m_j - m*) l_j are formed with shuffles, then out = sum_i w_i * acc_i with float4 loads
-// (lane c owns columns 4c..4c+3). Two dependent memory rounds when ns <= 32.
+// (lane c owns columns 4c..4c+3). Used for more than 32 splits.
 template <int D>
 __device__ void combine_head_long(const DecodeParams& p, int ns, size_t head, int lane, bool out_bf16) {
   constexpr int kVec = D / 4;
@@ -586,69 +586,86 @@ __device__ void combine_head_long(const DecodeParams& p, int ns, size_t head, in
   }
 }
 
-// Combine of up to 32 splits: the (max, sum) pair of split `lane` and the first batch of
-// partial rows are loaded together, so one head costs about one L2 round trip. Lane l covers
-// float4 column l % (D / 4) of rows l / (D / 4), l / (D / 4) + 32 / (D / 4), ...
-template <int D>
-__device__ void combine_head(const DecodeParams& p, int ns, size_t head, int lane, bool out_bf16) {
+// Combine of up to 32 split partials for kH consecutive query heads of one kv group (they share
+// the split count), by one warp: out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i with
+// M = max_i m_i. The (max, sum) pairs and the first kB * (32 / (D / 4)) partial rows of every
+// head are loaded at once, so a warp's heads cost about one L2 round trip. Split i's pair sits
+// in lane i; lane c covers float4 column c % (D / 4) of splits c / (D / 4), c / (D / 4) +
+// 32 / (D / 4), ...
+template <int D, int kH>
+__device__ void combine_heads(const DecodeParams& p, int ns, size_t head0, int lane, bool out_bf16) {
   constexpr int kVec = D / 4;
   constexpr int kRows = 32 / kVec;
-  constexpr int kBatch = 8;
-  if (ns > 32) {
-    combine_head_long<D>(p, ns, head, lane, out_bf16);
-    return;
-  }
-  const size_t slot0 = head * p.max_splits;
-  const float4* src = reinterpret_cast<const float4*>(p.part_o + slot0 * D);
+  constexpr int kB = 8;
   const int col = lane % kVec, row = lane / kVec;
-  float2 ml = make_float2(-INFINITY, 0.f);
-  if (lane < ns) ml = __ldcg(&p.part_ml[slot0 + lane]);
-  float4 v[kBatch];
+  float2 ml[kH];
+  float4 v[kH][kB], acc[kH];
+  float M[kH], w[kH], den[kH];
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int j = 0; j < kBatch; ++j) {
-    const int i = j * kRows + row;
-    v[j] = i < ns ? __ldcg(src + static_cast<size_t>(i) * kVec + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int h = 0; h < kH; ++h) {
+    const size_t slot0 = (head0 + h) * p.max_splits;
+    ml[h] = lane < ns ? __ldcg(&p.part_ml[slot0 + lane]) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const int j = k * kRows + row;
+      v[h][k] = j < ns ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot0 + j) * D) + col)
+                       : zero;
+    }
+    acc[h] = zero;
   }
-  float mstar = ml.x;
-  for (int off = 16; off; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-  const float e = (lane < ns && mstar != -INFINITY) ? ex2(ml.x - mstar) : 0.f;
-  float den = e * ml.y;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int i0 = 0; i0 < ns; i0 += kBatch * kRows) {
-    if (i0 > 0) {
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const int i = i0 + j * kRows + row;
-        v[j] = i < ns ? __ldcg(src + static_cast<size_t>(i) * kVec + col)
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int h = 0; h < kH; ++h) {
+    M[h] = ml[h].x;
+    for (int off = 16; off; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(0xffffffffu, M[h], off));
+    w[h] = (lane < ns && M[h] != -INFINITY) ? ex2(ml[h].x - M[h]) : 0.f;
+    den[h] = w[h] * ml[h].y;
+    for (int off = 16; off; off >>= 1) den[h] += __shfl_xor_sync(0xffffffffu, den[h], off);
+  }
+  for (int j0 = 0; j0 < ns; j0 += kB * kRows) {
+    if (j0 > 0) {
+#pragma unroll
+      for (int h = 0; h < kH; ++h) {
+        const size_t slot0 = (head0 + h) * p.max_splits;
+#pragma unroll
+        for (int k = 0; k < kB; ++k) {
+          const int j = j0 + k * kRows + row;
+          v[h][k] = j < ns ? __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot0 + j) * D) + col)
+                           : zero;
+        }
       }
     }
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int i = i0 + j * kRows + row;
-      const float ej = __shfl_sync(0xffffffffu, e, i & 31);
-      if (i < ns) {
-        acc.x = fmaf(ej, v[j].x, acc.x);
-        acc.y = fmaf(ej, v[j].y, acc.y);
-        acc.z = fmaf(ej, v[j].z, acc.z);
-        acc.w = fmaf(ej, v[j].w, acc.w);
+    for (int h = 0; h < kH; ++h) {
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        const int j = j0 + k * kRows + row;
+        const float wj = __shfl_sync(0xffffffffu, w[h], j & 31);
+        if (j < ns) {
+          acc[h].x = fmaf(wj, v[h][k].x, acc[h].x);
+          acc[h].y = fmaf(wj, v[h][k].y, acc[h].y);
+          acc[h].z = fmaf(wj, v[h][k].z, acc[h].z);
+          acc[h].w = fmaf(wj, v[h][k].w, acc[h].w);
+        }
       }
     }
   }
-  if (kRows == 2) {
-    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, 16);
-    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, 16);
-    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, 16);
-    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, 16);
-  }
-  for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  if (lane < kVec) {
-    const size_t o = head * D + 4 * lane;
-    store_out(p.out, o, acc.x * inv, out_bf16);
-    store_out(p.out, o + 1, acc.y * inv, out_bf16);
-    store_out(p.out, o + 2, acc.z * inv, out_bf16);
-    store_out(p.out, o + 3, acc.w * inv, out_bf16);
+#pragma unroll
+  for (int h = 0; h < kH; ++h) {
+    if (kRows == 2) {
+      acc[h].x += __shfl_xor_sync(0xffffffffu, acc[h].x, 16);
+      acc[h].y += __shfl_xor_sync(0xffffffffu, acc[h].y, 16);
+      acc[h].z += __shfl_xor_sync(0xffffffffu, acc[h].z, 16);
+      acc[h].w += __shfl_xor_sync(0xffffffffu, acc[h].w, 16);
+    }
+    const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;
+    if (lane < kVec) {
+      const size_t o = (head0 + h) * D + 4 * col;
+      store_out(p.out, o, acc[h].x * inv, out_bf16);
+      store_out(p.out, o + 1, acc[h].y * inv, out_bf16);
+      store_out(p.out, o + 2, acc[h].z * inv, out_bf16);
+      store_out(p.out, o + 3, acc[h].w * inv, out_bf16);
+    }
   }
 }
 
@@ -1109,12 +1126,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     __syncthreads();
     if (!*abort_flag) {
+      // one warp per kH query heads of a kv group (they share the sequence's split count);
+      // consecutive units go to different CTAs
+      constexpr int kH = G < 2 ? G : 2;
       const int nwarps = kDecodeThreads / 32;
-      const int heads = N * p.num_q_heads;
-      for (int h = blockIdx.x * nwarps + warp; h < heads; h += gridDim.x * nwarps) {
-        const int seq = h / p.num_q_heads;
+      const int units = N * (p.num_q_heads / kH);
+      for (int u = warp * gridDim.x + blockIdx.x; u < units; u += gridDim.x * nwarps) {
+        const size_t head0 = static_cast<size_t>(u) * kH;
+        const int seq = static_cast<int>(head0 / p.num_q_heads);
         const int ns = (pf1[seq + 1] - pf1[seq] + pf2[seq + 1] - pf2[seq]) / Hkv;  // 0: none
-        if (ns > 1) combine_head<D>(p, ns, static_cast<size_t>(h), lane, qbf);
+        if (ns > 32) {
+          for (int h = 0; h < kH; ++h) combine_head_long<D>(p, ns, head0 + h, lane, qbf);
+        } else if (ns > 1) {
+          combine_heads<D, kH>(p, ns, head0, lane, qbf);
+        }
       }
     }
   }
