@@ -693,8 +693,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(bp + p.off_bar);
   uint64_t* full = bar;                       // [kMaxStages] stage landed
   uint64_t* empty = bar + kMaxStages;         // [kMaxStages] stage consumed
-  uint64_t* qfull = bar + 2 * kMaxStages;     // [kItemSlots] item descriptor, table, queries ready
+  uint64_t* qfull = bar + 2 * kMaxStages;     // [kItemSlots] item descriptor and table written
   uint64_t* qempty = qfull + kItemSlots;      // [kItemSlots] slot released by producers + consumers
+  uint64_t* qland = qempty + kItemSlots;      // [kItemSlots] item queries landed (bulk copy)
+  uint64_t* sorted = qland + kItemSlots;      // [1] part-2 order written by the consumer warps
   uint32_t* meta = reinterpret_cast<uint32_t*>(bp + p.off_meta);     // [kMaxStages] valid tokens
   ItemDesc* items = reinterpret_cast<ItemDesc*>(bp + p.off_items);  // [kItemSlots]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(items + kItemSlots);
@@ -754,7 +756,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int b = 0; b < kItemSlots; ++b) {
         mbar_init(smem_addr(qfull + b), 1);
         mbar_init(smem_addr(qempty + b), kProducerWarps + kConsumerWarps);
+        mbar_init(smem_addr(qland + b), 1);
       }
+      mbar_init(smem_addr(sorted), 1);
       fence_barrier_init();
     }
     // block-wide exclusive scan of (c1, c2): warp scans, then a scan of the warp totals
@@ -813,39 +817,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     __syncthreads();
   }
-  // part 2 order: chunks of kDecodeThreads sequences; a sequence's position is its bucket's
-  // start, plus the bucket's sequences in earlier warps, plus those in earlier lanes
-  for (int c0 = 0; c0 < N; c0 += kDecodeThreads) {
-    const int s = c0 + tid;
-    const int b = s < N ? rem_bucket(__ldg(p.ctx_lens + s)) : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, b);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    if (b >= 0 && rank == 0) wcnt[warp * kRemBuckets + b] = __popc(peers);
-    __syncthreads();
-    if (b >= 0) {
-      int pos = bstart[b] + rank;
-      for (int w = 0; w < warp; ++w) pos += wcnt[w * kRemBuckets + b];
-      order2[pos] = s;
-    }
-    __syncthreads();
-    if (tid < kRemBuckets) {
-      int add = 0;
-      for (int w = 0; w < kScanWarps; ++w) {
-        add += wcnt[w * kRemBuckets + tid];
-        wcnt[w * kRemBuckets + tid] = 0;
-      }
-      bstart[tid] += add;
-    }
-    __syncthreads();
-  }
   const int items1 = pf1[N];
   const int total_items = items1 + pf2[N];
 
   if (warp == 0) {
     // ------------------------------------------------------------------ scheduler warp
-    // Takes items from the global counter in sequence order and fills the item slots:
-    // descriptor, the item's block-table slice (validated) and, by bulk copy, its queries.
+    // Takes items from the global counter and fills the item slots: descriptor, the item's
+    // block-table slice (validated) and, by bulk copy, its queries.
     const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
+    bool have_order = false;  // lane 0: the consumers' part-2 order is complete
     for (uint32_t it = 0;; ++it) {
       const int slot = it % kItemSlots;
       if (it >= kItemSlots &&
@@ -858,7 +838,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       int item = 0, seq = 0;
       if (lane == 0) {
-        item = static_cast<int>(fetch_ticket(p.counters, p.launch_id));
+        // the first item of CTA b is item b; the counter hands out the rest
+        item = it == 0 ? static_cast<int>(blockIdx.x)
+                       : static_cast<int>(gridDim.x + fetch_ticket(p.counters, p.launch_id));
+        if (item >= items1 && item < total_items && !have_order) {
+          have_order = mbar_wait_bounded(smem_addr(sorted), 0);
+          if (!have_order) {
+            flag_error(p.err, kErrTimeout);
+            *abort_flag = 1;
+          }
+        }
         if (item < items1) {
           int lo = 0, hi = N - 1;  // largest s with pf1[s] <= item
           while (lo < hi) {
@@ -915,12 +904,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         d.tok0 = tok0;
         d.tok_end = tok_end;
         d.nblk = nblk;
-        const uint32_t qf = smem_addr(qfull + slot);
-        mbar_arrive_expect_tx(qf, qbytes);
+        // descriptor and table for the producers now, the queries for the consumers on landing
+        mbar_arrive(smem_addr(qfull + slot));
+        const uint32_t ql = smem_addr(qland + slot);
+        mbar_arrive_expect_tx(ql, qbytes);
         bulk_copy_g2s(smem_addr(qbuf + slot * G * D),
                       static_cast<const uint16_t*>(p.q) +
                           (static_cast<size_t>(seq) * p.num_q_heads + kvh * G) * D,
-                      qbytes, qf);
+                      qbytes, ql);
       }
     }
   } else if (warp <= kProducerWarps) {
@@ -1023,10 +1014,39 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int cw = warp - kFirstConsumer;
     const int ctid = tid - kFirstConsumer * 32;
     Consumer<KV, D, G, kMma> c;
+    // Part-2 order (the scheduler needs it only once part 1 is handed out): chunks of
+    // kConsumerThreads sequences; a sequence's position is its bucket's start, plus the
+    // bucket's sequences in earlier consumer warps of the chunk, plus those in earlier lanes.
+    for (int c0 = 0; c0 < N; c0 += kConsumerThreads) {
+      const int s = c0 + ctid;
+      const int b = s < N ? rem_bucket(__ldg(p.ctx_lens + s)) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, b);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (b >= 0 && rank == 0) wcnt[cw * kRemBuckets + b] = __popc(peers);
+      bar_sync(1, kConsumerThreads);
+      if (b >= 0) {
+        int pos = bstart[b] + rank;
+        for (int w = 0; w < cw; ++w) pos += wcnt[w * kRemBuckets + b];
+        order2[pos] = s;
+      }
+      bar_sync(1, kConsumerThreads);
+      if (ctid < kRemBuckets) {
+        int add = 0;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          add += wcnt[w * kRemBuckets + ctid];
+          wcnt[w * kRemBuckets + ctid] = 0;
+        }
+        bstart[ctid] += add;
+      }
+      bar_sync(1, kConsumerThreads);
+    }
+    if (ctid == 0) mbar_arrive(smem_addr(sorted));
     uint32_t g0 = 0;
     for (uint32_t it = 0;; ++it) {
       const int slot = it % kItemSlots;
-      const bool got = mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1);
+      bool got = mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1);
+      const ItemDesc d = items[slot];
+      if (got && d.seq >= 0) got = mbar_wait_bounded(smem_addr(qland + slot), (it / kItemSlots) & 1);
       if (bar_or(kConsumerThreads, !got)) {  // every consumer warp leaves together
         if (ctid == 0) {
           flag_error(p.err, kErrTimeout);
@@ -1034,7 +1054,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         }
         break;
       }
-      const ItemDesc d = items[slot];
       if (d.seq < 0) break;
       c.init(qbuf + slot * G * D, qbf, lane);
       float score_scale = p.score_scale;

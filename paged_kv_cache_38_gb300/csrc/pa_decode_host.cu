@@ -194,7 +194,7 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   const size_t merge = static_cast<size_t>(kConsumerWarps) * group * D * 4 +
                        static_cast<size_t>(kConsumerWarps) * group * 8;
   const size_t qbytes = static_cast<size_t>(kItemSlots) * group * D * 2;
-  const size_t bars = (2 * kMaxStages + 2 * kItemSlots) * 8;
+  const size_t bars = (2 * kMaxStages + 3 * kItemSlots + 1) * 8;
   const size_t meta = kMaxStages * 4;
   const size_t items = kItemSlots * sizeof(ItemDesc) + 16;
   pl.tbl_stride = ((tbl_entries + 3) / 4) * 4;
