@@ -97,6 +97,11 @@ class Oracle:
         lib.pao_swap_blocks.argtypes = [_ptr, _ptr, _c_int, _ptr, _ptr, _c_int, _c_int,
                                         ctypes.c_size_t, _c_int]
         lib.pao_max_threads.restype = _c_int
+        lib.pao_e4m3_encode_array.restype = None
+        lib.pao_e4m3_encode_array.argtypes = [_ptr, _ptr, ctypes.c_size_t]
+        lib.pao_write_kv_fp8.restype = _c_int
+        lib.pao_write_kv_fp8.argtypes = [_ptr, _ptr, _c_int, _ptr, _ptr, _ptr] + [_c_int] * 5 + [
+            ctypes.c_float, ctypes.c_float]
         self.lib = lib
 
     # -------------------------------------------------------------- number formats
@@ -106,6 +111,13 @@ class Oracle:
               "e4m3": self.lib.pao_e4m3_value}[dtype]
         flat = np.asarray(bits).reshape(-1)
         return np.array([fn(int(b)) for b in flat], dtype=np.float64).reshape(np.shape(bits))
+
+    def e4m3_encode(self, x) -> np.ndarray:
+        """E4M3 codes (uint8) of float32 values: nearest, ties to even, saturating, NaN -> 0x7F."""
+        xf = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+        out = np.empty(xf.shape, dtype=np.uint8)
+        self.lib.pao_e4m3_encode_array(_p(xf), _p(out), xf.size)
+        return out
 
     def max_threads(self) -> int:
         return int(self.lib.pao_max_threads())
@@ -145,6 +157,20 @@ class Oracle:
         return int(self.lib.pao_write_kv(_p(kb), _p(vb), _p(k_pool), _p(v_pool), _p(sm),
                                          sm.shape[0], num_kv_heads, head_dim, block_size,
                                          k_pool.size // per_block, DTYPES[kv_dtype]))
+
+    def write_kv_fp8(self, k, v, k_pool: np.ndarray, v_pool: np.ndarray, slot_mapping, *,
+                     src_dtype: str, num_kv_heads: int, head_dim: int, block_size: int,
+                     k_scale: float, v_scale: float) -> int:
+        """Quantise-on-write into uint8 E4M3 pools, in place; returns 0 or -1 (a bad slot)."""
+        kb, vb = _raw(k), _raw(v)
+        sm = _int_array(slot_mapping, np.int64).reshape(-1)
+        assert k_pool.dtype == np.uint8 and k_pool.flags.c_contiguous
+        assert v_pool.dtype == np.uint8 and v_pool.flags.c_contiguous
+        per_block = num_kv_heads * block_size * head_dim
+        return int(self.lib.pao_write_kv_fp8(_p(kb), _p(vb), DTYPES[src_dtype], _p(k_pool),
+                                             _p(v_pool), _p(sm), sm.shape[0], num_kv_heads,
+                                             head_dim, block_size, k_pool.size // per_block,
+                                             float(k_scale), float(v_scale)))
 
     def copy_blocks(self, k_pools: Sequence[np.ndarray], v_pools: Sequence[np.ndarray], pairs,
                     *, block_bytes: int) -> int:

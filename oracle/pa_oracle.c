@@ -18,6 +18,8 @@
  *         blocks).
  *  [CB]   "Continuous Batching and PagedAttention", section "The block table is a page table"
  *         (attention math unchanged; gather through the table).
+ *  [PV]   "KV Cache Preemption in vLLM: Swap, Recompute and Behavior Under Memory Pressure",
+ *         section "How much KV cache a token costs" (an FP8 cache holds one byte per element).
  *  Number formats (the pages name FP16 and FP8 but do not define them): IEEE 754 binary16,
  *  bfloat16 (binary32 with the low 16 fraction bits dropped) and OCP 8-bit floating point
  *  E4M3 (bias 7, no infinities, S.1111.111 = NaN).
@@ -27,7 +29,8 @@
  *  - ctx_len counts every filled slot including the token written this step;
  *  - GQA groups are contiguous: query head h reads kv head h / (Hq / Hkv);
  *  - ctx_len == 0 gives an all-zero output row;
- *  - FP8 values are dequantised as (stored value) * per-tensor scale.
+ *  - FP8 values are dequantised as (stored value) * per-tensor scale, and quantised on write as
+ *    the nearest E4M3 code (ties to even, saturating at 448) of value / scale.
  *
  * Parity pins: every function here is pinned by tests against library decoders, a library
  * attention routine on the unpaged data, closed forms and the worked example of [P1].
@@ -93,6 +96,42 @@ double pao_e4m3_value(uint8_t bits) {
     mag = ldexp((double)(8 + f), e - 7 - 3); /* (1 + f / 2^3) * 2^(e - 7) */
   }
   return sign ? -mag : mag;
+}
+
+/* Round to the nearest integer, ties to the even one, of a value 0 <= m < 2^31. */
+static uint32_t round_half_even(double m) {
+  const double f = floor(m);
+  const double r = m - f;
+  uint32_t q = (uint32_t)f;
+  if (r > 0.5 || (r == 0.5 && (q & 1u))) ++q;
+  return q;
+}
+
+/* The E4M3 code nearest to x, ties to the code with an even fraction field; magnitudes at or
+ * beyond the largest finite value 448 (infinities included) saturate to it, NaN gives the NaN
+ * code 0x7F. Subnormal codes are the multiples of 2^-9 below 2^-6. */
+uint8_t pao_e4m3_encode(float x) {
+  if (isnan(x)) return 0x7F;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* q = 8 rounds up to 2^-6, whose code (exponent field 1, fraction 0) is also 8 */
+    return sign | (uint8_t)round_half_even(ldexp(a, 9));
+  }
+  int e;
+  frexp(a, &e); /* a = f * 2^e, f in [0.5, 1), so a = (1 + m / 8) * 2^(e - 1) */
+  int E = e - 1;
+  uint32_t q = round_half_even((ldexp(a, -E) - 1.0) * 8.0);
+  if (q == 8) { /* rounded up to the next power of two */
+    q = 0;
+    E += 1;
+  }
+  return sign | (uint8_t)(((E + 7) << 3) | q);
+}
+
+void pao_e4m3_encode_array(const float* x, uint8_t* out, size_t n) {
+  for (size_t i = 0; i < n; ++i) out[i] = pao_e4m3_encode(x[i]);
 }
 
 /* Threads the OpenMP runtime would use (1 when built without OpenMP). */
@@ -228,6 +267,41 @@ int pao_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
       const size_t src = ((size_t)t * num_kv_heads + h) * row;
       memcpy((uint8_t*)k_pool + dst, (const uint8_t*)k + src, row);
       memcpy((uint8_t*)v_pool + dst, (const uint8_t*)v + src, row);
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/*
+ * Quantise-on-write into an FP8 cache ([PV] section "How much KV cache a token costs": one byte
+ * per element): each new K or V element x, given in f16 or bf16, is stored as the E4M3 code of
+ * x / scale (k_scale for K, v_scale for V), so that code * scale recovers it. The quotient is
+ * the binary32 quotient rounded to nearest: the fp64 quotient of the two binary32 values,
+ * rounded once to float, is exactly that. Slots as in pao_write_kv. Returns -1 if a slot lies
+ * outside the pool (that token is skipped).
+ */
+int pao_write_kv_fp8(const void* k, const void* v, int src_dtype, void* k_pool, void* v_pool,
+                     const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                     int block_size, int num_blocks, float k_scale, float v_scale) {
+  int bad = 0;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t sigma = slot_mapping[t];
+    if (sigma < 0) continue;
+    const int64_t blk = sigma / block_size;
+    const int64_t slot = sigma % block_size;
+    if (blk >= num_blocks) {
+      bad = 1;
+      continue;
+    }
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + slot) * head_dim;
+      const size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+      for (int d = 0; d < head_dim; ++d) {
+        const float qk = (float)(element(k, src + d, src_dtype) / (double)k_scale);
+        const float qv = (float)(element(v, src + d, src_dtype) / (double)v_scale);
+        ((uint8_t*)k_pool)[dst + d] = pao_e4m3_encode(qk);
+        ((uint8_t*)v_pool)[dst + d] = pao_e4m3_encode(qv);
+      }
     }
   }
   return bad ? -1 : 0;

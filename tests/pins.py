@@ -2,7 +2,8 @@
 
 Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError when the oracle
 disagrees with
-  * a library decoder (numpy float16, torch bfloat16 / float8_e4m3fn) or the OCP E4M3 table,
+  * a library decoder or encoder (numpy float16, torch bfloat16 / float8_e4m3fn) or the OCP
+    E4M3 table,
   * a library attention routine (torch scaled_dot_product_attention in fp64, with its own GQA
     grouping) run on the unpaged keys and values the generator kept,
   * closed forms (one token, equal keys, zero scale, one dominant key, empty context),
@@ -129,6 +130,41 @@ def pin_e4m3_decoder(orc):
                 assert math.isnan(val), b
             else:
                 assert val == float(v) and math.copysign(1, val) == math.copysign(1, float(v)), b
+
+
+def _e4m3_library(q: np.ndarray) -> np.ndarray:
+    """E4M3 codes by the library cast. torch rounds to nearest-even but turns magnitudes beyond
+    the largest finite value into NaN, so values are clamped to +-448 first: the saturating
+    reading of the FP8 cache. NaN inputs give a NaN code of either sign."""
+    t = torch.from_numpy(np.ascontiguousarray(q, dtype=np.float32))
+    return t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_encoder(orc):
+    """Every bf16 and f16 value, divided by several scales in binary32, encodes as the library
+    cast does; decoding then encoding every code gives the code back; the midpoint of two
+    neighbouring codes goes to the one with the even fraction field."""
+    bits = np.arange(65536, dtype=np.uint16)
+    bf = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float32).numpy()
+    hf = bits.view(np.float16).astype(np.float32)
+    for vals in (bf, hf):
+        for sc in (1.0, 0.0078125, 0.37, 3.3e-3, 170.0):
+            q = (vals / np.float32(sc)).astype(np.float32)
+            got = orc.e4m3_encode(q)
+            ref = _e4m3_library(q)
+            nan = np.isnan(q)
+            assert np.all(got[nan] == 0x7F), "NaN must give the NaN code"
+            assert np.array_equal(got[~nan], ref[~nan]), f"E4M3 encoding differs, scale {sc}"
+    codes = np.arange(256, dtype=np.uint8)
+    vals = orc.value(codes, "e4m3")
+    ok = ~np.isnan(vals)
+    assert np.array_equal(orc.e4m3_encode(vals[ok].astype(np.float32)), codes[ok])
+    pos = vals[:0x7F]                       # codes 0x00..0x7E, increasing
+    mid = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)  # exact in binary32
+    lo = np.arange(0x7E)
+    want = np.where(lo % 2 == 0, lo, lo + 1).astype(np.uint8)
+    assert np.array_equal(orc.e4m3_encode(mid), want), "ties must go to the even code"
+    assert np.array_equal(orc.e4m3_encode(-mid), want | 0x80)
 
 
 # ------------------------------------------------------------------ attention
@@ -270,6 +306,51 @@ def pin_write_kv(orc):
                           num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
                           block_size=B, kv_dtype=spec.kv_dtype)
         assert rc == -1 and np.array_equal(kp, ref_k)
+
+
+def pin_write_kv_fp8(orc):
+    """Quantise-on-write stores in each new token's slot the library-cast E4M3 code of
+    value / scale (binary32 quotient): the same pools as quantising first and then writing the
+    bytes with the pinned raw write_kv. Specials included: signed zeros, infinities, values
+    beyond 448, f16 subnormals, NaN."""
+    specials = [0.0, -0.0, math.inf, -math.inf, 1.0e4, -1.0e4, 3.0e-6, math.nan]
+    for i, src in enumerate(("bf16", "f16")):
+        spec = synth.DecodeSpec(f"q8_{src}", 6, 8, 2, 64, 8, "e4m3", src, ctx_range=(1, 40))
+        case = synth.make_case(spec, seed=71 + i)
+        dt = torch.bfloat16 if src == "bf16" else torch.float16
+        g = torch.Generator().manual_seed(5 + i)
+        shape = (spec.num_seqs, spec.num_kv_heads, spec.head_dim)
+        kn = (torch.randn(shape, generator=g) * 3).to(dt)
+        vn = (torch.randn(shape, generator=g) * 0.2).to(dt)
+        kn.view(-1)[: len(specials)] = torch.tensor(specials).to(dt)
+        vn.view(-1)[-len(specials):] = torch.tensor(specials).to(dt)
+        ks, vs = 0.05, 0.3
+        kp, vp = _raw_u8(case.k_pool), _raw_u8(case.v_pool)
+        kp2, vp2 = kp.copy(), vp.copy()
+        sm = torch.cat([case.slot_mapping, torch.tensor([-1], dtype=torch.int64)])
+        kn_p = torch.cat([kn, kn[:1]])
+        vn_p = torch.cat([vn, vn[:1]])
+        rc = orc.write_kv_fp8(kn_p, vn_p, kp, vp, sm, src_dtype=src,
+                              num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                              block_size=spec.block_size, k_scale=ks, v_scale=vs)
+        assert rc == 0
+
+        def quant(t, sc):
+            q = t.to(torch.float32).numpy() / np.float32(sc)
+            codes = _e4m3_library(q)
+            codes[np.isnan(q)] = 0x7F
+            return codes
+
+        rc = orc.write_kv(quant(kn_p, ks), quant(vn_p, vs), kp2, vp2, sm,
+                          num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                          block_size=spec.block_size, kv_dtype="e4m3")
+        assert rc == 0
+        assert np.array_equal(kp, kp2) and np.array_equal(vp, vp2), src
+        bad = torch.tensor([case.num_blocks * spec.block_size], dtype=torch.int64)
+        rc = orc.write_kv_fp8(kn[:1], vn[:1], kp, vp, bad, src_dtype=src,
+                              num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                              block_size=spec.block_size, k_scale=ks, v_scale=vs)
+        assert rc == -1 and np.array_equal(kp, kp2)
 
 
 def _toy_script():
@@ -429,5 +510,5 @@ ALL_PINS = [
     pin_f16_decoder, pin_bf16_decoder, pin_e4m3_decoder, pin_paged_equals_library_attention,
     pin_closed_forms, pin_scales, pin_group_equals_replicated_heads, pin_permutation_invariance,
     pin_bounds, pin_write_kv, pin_toy_figures, pin_toy_permuted, pin_copy_on_write,
-    pin_swap_round_trip,
+    pin_swap_round_trip, pin_e4m3_encoder, pin_write_kv_fp8,
 ]

@@ -40,7 +40,7 @@ MUTANTS = [
     ("f16_subnormal_scale", "mag = ldexp((double)f, -24);", "mag = ldexp((double)f, -25);", 1),
     ("f16_sign_ignored", "return sign ? -mag : mag;\n}\n\n/* bfloat16",
      "return mag;\n}\n\n/* bfloat16", 1),
-    ("write_slot_zero", "const int64_t slot = sigma % block_size;", "const int64_t slot = 0;", 1),
+    ("write_slot_zero", "const int64_t slot = sigma % block_size;", "const int64_t slot = 0;", 2),
     ("write_v_from_k", "memcpy((uint8_t*)v_pool + dst, (const uint8_t*)v + src, row);",
      "memcpy((uint8_t*)v_pool + dst, (const uint8_t*)k + src, row);", 1),
     ("write_head_stride_dropped",
@@ -55,6 +55,16 @@ MUTANTS = [
      "(((size_t)i * num_layers + l) * 2 + 0) * block_bytes", 1),
     ("swap_layer_major", "(((size_t)i * num_layers + l) * 2",
      "(((size_t)l * n + i) * 2", 2),
+    ("encode_truncates", "if (r > 0.5 || (r == 0.5 && (q & 1u))) ++q;", "", 1),
+    ("encode_ties_away", "(r == 0.5 && (q & 1u))", "(r == 0.5)", 1),
+    ("encode_no_saturation", "if (a >= 448.0) return sign | 0x7E;",
+     "if (a >= 480.0) return sign | 0x7F;", 1),
+    ("encode_bias_8", "((E + 7) << 3)", "((E + 8) << 3)", 1),
+    ("encode_subnormal_step", "round_half_even(ldexp(a, 9))", "round_half_even(ldexp(a, 8))", 1),
+    ("encode_sign_dropped", "return sign | (uint8_t)(((E + 7) << 3) | q);",
+     "return (uint8_t)(((E + 7) << 3) | q);", 1),
+    ("quantise_multiplies", "/ (double)k_scale", "* (double)k_scale", 1),
+    ("quantise_v_with_k_scale", "/ (double)v_scale", "/ (double)k_scale", 1),
 ]
 
 
