@@ -449,6 +449,35 @@ def run_extras(args, dev, flush, peaks) -> dict:
         torch.cuda.empty_cache()
     res["preemption_swap"] = run_swap_bench(dev)
     res["copy_blocks_large"] = run_copy_bench(dev, flush, peaks)
+    res["write_kv_fp8"] = run_quantise_bench(dev, flush, peaks)
+    return res
+
+
+def run_quantise_bench(dev, flush, peaks) -> dict:
+    """pa_write_kv_fp8 (bf16 in, E4M3 pool) for a prefill-sized batch of 32,768 tokens of the
+    FP8 workload's geometry (8 kv heads x 128), plus the 256-token decode step as a latency."""
+    import paged_kv_cache_38_gb300 as pa
+
+    hkv, d, b, ntok = 8, 128, 16, 32768
+    nblk = ntok // b + 64
+    g = torch.Generator(device=dev).manual_seed(SEED)
+    k = torch.randn(ntok, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn(ntok, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    kp = torch.empty(nblk, hkv, b, d, dtype=torch.uint8, device=dev)
+    vp = torch.empty_like(kp)
+    slots = torch.from_numpy(np.random.default_rng(SEED).permutation(nblk * b)[:ntok]).to(dev)
+    ks, vs = float(k.float().abs().max()) / 448.0, float(v.float().abs().max()) / 448.0
+    call = lambda n: pa.pa_write_kv_fp8(k[:n], v[:n], kp, vp, slots[:n], ks, vs)  # noqa: E731
+    call(ntok)
+    t = statistics.mean(time_steps(lambda: call(ntok), 10, flush))
+    t_small = statistics.mean(time_steps(lambda: call(256), 20, flush))
+    byts = ntok * (2 * hkv * d * 2 + 2 * hkv * d + 8)  # bf16 read, E4M3 written, slot read
+    gbs = byts / (t * 1e-3) / 1e9
+    res = {"tokens": ntok, "bytes": byts, "ms": round(t, 4), "gbs": round(gbs, 1),
+           "pct_of_peak": round(100 * gbs / peaks["hbm_gbs"], 1),
+           "step_256_tokens_us": round(t_small * 1e3, 2)}
+    del k, v, kp, vp
+    torch.cuda.empty_cache()
     return res
 
 

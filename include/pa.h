@@ -157,6 +157,31 @@ pa_status pa_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
                       int32_t* err_flag, pa_stream stream);
 
 /*
+ * pa_write_kv_fp8 - store each new token's key and value, given in f16 or bf16, in an E4M3
+ * pool (quantise on write).
+ *
+ * Source: "KV Cache Preemption in vLLM: Swap, Recompute and Behavior Under Memory Pressure",
+ * section "How much KV cache a token costs" (an FP8 cache stores one byte per element, half of
+ * FP16) and section "What to do next" (switch the cache to FP8); slots as in pa_write_kv. For
+ * every token t with sigma = slot_mapping[t] >= 0, kv head h and element d:
+ *     k_pool[sigma / block_size][h][sigma % block_size][d] = E4M3(k[t][h][d] * (1 / k_scale))
+ * (same for v with v_scale), where 1 / k_scale and the product are rounded to nearest binary32
+ * (the pages give no rounding for this step; this is the usual form) and E4M3(x) is the nearest
+ * OCP E4M3 code, ties to the even code, magnitudes at or beyond 448 (infinities included)
+ * saturating to +-448, NaN giving a NaN code. pa_decode with the same k_scale / v_scale
+ * dequantises code * scale. Bad or padding slots as in pa_write_kv.
+ *   k, v          device [num_tokens][num_kv_heads][head_dim], src_dtype (PA_F16 or PA_BF16),
+ *                 16-byte aligned
+ *   k_pool,v_pool device E4M3 pools, layout above, 16-byte aligned
+ *   k_scale,v_scale  finite and > 0 (PA_EINVAL otherwise); head_dim a multiple of 16
+ */
+pa_status pa_write_kv_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_pool,
+                          void* v_pool, const int64_t* slot_mapping, int32_t num_tokens,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, float k_scale, float v_scale, int32_t* err_flag,
+                          pa_stream stream);
+
+/*
  * pa_copy_blocks - copy-on-write duplication of whole physical blocks.
  *
  * Source: PagedAttention summary page, paragraph on sharing (a sample that must write into a

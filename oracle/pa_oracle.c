@@ -30,7 +30,8 @@
  *  - GQA groups are contiguous: query head h reads kv head h / (Hq / Hkv);
  *  - ctx_len == 0 gives an all-zero output row;
  *  - FP8 values are dequantised as (stored value) * per-tensor scale, and quantised on write as
- *    the nearest E4M3 code (ties to even, saturating at 448) of value / scale.
+ *    the nearest E4M3 code (ties to even, saturating at 448) of value * (1 / scale), both the
+ *    reciprocal and the product rounded to binary32.
  *
  * Parity pins: every function here is pinned by tests against library decoders, a library
  * attention routine on the unpaged data, closed forms and the worked example of [P1].
@@ -275,14 +276,18 @@ int pao_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
 /*
  * Quantise-on-write into an FP8 cache ([PV] section "How much KV cache a token costs": one byte
  * per element): each new K or V element x, given in f16 or bf16, is stored as the E4M3 code of
- * x / scale (k_scale for K, v_scale for V), so that code * scale recovers it. The quotient is
- * the binary32 quotient rounded to nearest: the fp64 quotient of the two binary32 values,
- * rounded once to float, is exactly that. Slots as in pao_write_kv. Returns -1 if a slot lies
- * outside the pool (that token is skipped).
+ * x * inv, with inv = 1 / scale rounded to binary32 (k_scale for K, v_scale for V), so that
+ * code * scale recovers it; the product is rounded to binary32 first. The pages give no rounding
+ * for this step; multiplying by the binary32 reciprocal is the usual form. In fp64 the product
+ * of two binary32 values is exact, so rounding it once to float gives the binary32 product, and
+ * rounding 1 / scale from fp64 to float gives the correctly rounded reciprocal. Slots as in
+ * pao_write_kv. Returns -1 if a slot lies outside the pool (that token is skipped).
  */
 int pao_write_kv_fp8(const void* k, const void* v, int src_dtype, void* k_pool, void* v_pool,
                      const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
                      int block_size, int num_blocks, float k_scale, float v_scale) {
+  const float k_inv = (float)(1.0 / (double)k_scale);
+  const float v_inv = (float)(1.0 / (double)v_scale);
   int bad = 0;
   for (int t = 0; t < num_tokens; ++t) {
     const int64_t sigma = slot_mapping[t];
@@ -297,8 +302,8 @@ int pao_write_kv_fp8(const void* k, const void* v, int src_dtype, void* k_pool, 
       const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + slot) * head_dim;
       const size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
       for (int d = 0; d < head_dim; ++d) {
-        const float qk = (float)(element(k, src + d, src_dtype) / (double)k_scale);
-        const float qv = (float)(element(v, src + d, src_dtype) / (double)v_scale);
+        const float qk = (float)(element(k, src + d, src_dtype) * (double)k_inv);
+        const float qv = (float)(element(v, src + d, src_dtype) * (double)v_inv);
         ((uint8_t*)k_pool)[dst + d] = pao_e4m3_encode(qk);
         ((uint8_t*)v_pool)[dst + d] = pao_e4m3_encode(qv);
       }

@@ -71,6 +71,19 @@ pa_status pa_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
                 msg);
 }
 
+pa_status pa_write_kv_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_pool,
+                          void* v_pool, const int64_t* slot_mapping, int32_t num_tokens,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, float k_scale, float v_scale, int32_t* err_flag,
+                          pa_stream stream) {
+  std::string msg;
+  return finish(pa::run_write_kv_fp8(k, v, src_dtype, k_pool, v_pool, slot_mapping, num_tokens,
+                                     num_kv_heads, head_dim, block_size, num_blocks, k_scale,
+                                     v_scale, err_flag, reinterpret_cast<cudaStream_t>(stream),
+                                     msg),
+                msg);
+}
+
 pa_status pa_copy_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
                          const int32_t* pairs, int32_t num_pairs, int32_t num_blocks,
                          size_t block_bytes, int32_t* err_flag, pa_stream stream) {

@@ -7,8 +7,13 @@
 // copy-on-write; "KV Cache Preemption in vLLM", section "Swap versus recompute" (pinned memory,
 // a block's data is spread over every layer, so a swap moves 2 * layers slabs per block).
 //
-// All three are byte moves: 16-byte vector loads and stores, several in flight per thread.
+// All three are byte moves: 16-byte vector loads and stores, several in flight per thread. The
+// quantise-on-write variant of the write ("KV Cache Preemption in vLLM", section "How much KV
+// cache a token costs": an FP8 cache holds one byte per element) converts on the way.
+#include <cuda_fp16.h>
+
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "pa_device.cuh"
@@ -62,6 +67,84 @@ __global__ void __launch_bounds__(256) pa_write_kv_kernel(const __grid_constant_
     const uint4 vv = __ldg(p.v + src);
     p.k_pool[dst] = kv;
     p.v_pool[dst] = vv;
+  }
+}
+
+// ------------------------------------------------------------------ quantise-on-write (E4M3)
+
+struct WriteFp8Params {
+  const uint4* k;   // 16-bit rows: two 16-byte vectors per chunk of 16 elements
+  const uint4* v;
+  uint4* k_pool;    // E4M3 rows: one 16-byte vector per chunk
+  uint4* v_pool;
+  const int64_t* slots;
+  int32_t* err;
+  float k_scale, v_scale;
+  int src_bf16;
+  int num_tokens, num_kv_heads, chunks_per_row, block_size, num_blocks;
+};
+
+// Two binary32 values to two E4M3 codes, nearest / ties-to-even, saturating to +-448 (NaN stays
+// NaN); `first` lands in the low byte, which comes first in memory.
+__device__ __forceinline__ uint32_t e4m3x2(float first, float second) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+  return r;
+}
+
+// Eight 16-bit values (one 16-byte vector) times rcp = RN(1 / scale), rounded to binary32, as
+// eight E4M3 codes.
+__device__ __forceinline__ uint2 quantise8(uint4 w, float rcp, bool bf16) {
+  const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+  float f[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (bf16) {
+      f[2 * i] = __uint_as_float(words[i] << 16);
+      f[2 * i + 1] = __uint_as_float(words[i] & 0xffff0000u);
+    } else {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&words[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  uint32_t pk[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) pk[i] = e4m3x2(__fmul_rn(f[2 * i], rcp), __fmul_rn(f[2 * i + 1], rcp));
+  uint2 r;
+  r.x = pk[0] | (pk[1] << 16);
+  r.y = pk[2] | (pk[3] << 16);
+  return r;
+}
+
+// One thread per 16-element chunk of one (token, kv head) row.
+__global__ void __launch_bounds__(256) pa_write_kv_fp8_kernel(const __grid_constant__ WriteFp8Params p) {
+  const long long total =
+      static_cast<long long>(p.num_tokens) * p.num_kv_heads * p.chunks_per_row;
+  const bool bf16 = p.src_bf16 != 0;
+  const float k_rcp = __frcp_rn(p.k_scale), v_rcp = __frcp_rn(p.v_scale);  // IEEE reciprocals
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i % p.chunks_per_row);
+    const long long th = i / p.chunks_per_row;
+    const int h = static_cast<int>(th % p.num_kv_heads);
+    const int t = static_cast<int>(th / p.num_kv_heads);
+    const long long slot = __ldg(p.slots + t);
+    if (slot < 0) continue;  // padding token
+    const long long blk = slot / p.block_size;
+    if (blk >= p.num_blocks) {
+      if (h == 0 && c == 0) flag_error(p.err, kErrBlockId);
+      continue;
+    }
+    const long long src = 2 * (th * p.chunks_per_row + c);
+    const long long dst =
+        ((blk * p.num_kv_heads + h) * p.block_size + slot % p.block_size) * p.chunks_per_row + c;
+    const uint4 k0 = __ldg(p.k + src), k1 = __ldg(p.k + src + 1);
+    const uint4 v0 = __ldg(p.v + src), v1 = __ldg(p.v + src + 1);
+    const uint2 kq0 = quantise8(k0, k_rcp, bf16), kq1 = quantise8(k1, k_rcp, bf16);
+    const uint2 vq0 = quantise8(v0, v_rcp, bf16), vq1 = quantise8(v1, v_rcp, bf16);
+    p.k_pool[dst] = make_uint4(kq0.x, kq0.y, kq1.x, kq1.y);
+    p.v_pool[dst] = make_uint4(vq0.x, vq0.y, vq1.x, vq1.y);
   }
 }
 
@@ -211,6 +294,59 @@ pa_status run_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
                                                         std::max(1, device_sm_count()) * 8LL));
   pa_write_kv_kernel<<<grid, 256, 0, stream>>>(p);
   return cuda_status(cudaGetLastError(), "pa_write_kv launch", msg);
+}
+
+pa_status run_write_kv_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_pool,
+                           void* v_pool, const int64_t* slot_mapping, int32_t num_tokens,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                           int32_t num_blocks, float k_scale, float v_scale, int32_t* err_flag,
+                           cudaStream_t stream, std::string& msg) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0) {
+    msg = "sizes must be positive (num_tokens may be 0)";
+    return PA_EINVAL;
+  }
+  if (src_dtype != PA_F16 && src_dtype != PA_BF16) {
+    msg = "src_dtype must be PA_F16 or PA_BF16";
+    return PA_EINVAL;
+  }
+  if (head_dim % 16 != 0) {
+    msg = "head_dim must be a multiple of 16";
+    return PA_EINVAL;
+  }
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale)) {
+    msg = "k_scale and v_scale must be finite and > 0";
+    return PA_EINVAL;
+  }
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_pool || !v_pool || !slot_mapping) {
+    msg = "null pointer argument";
+    return PA_EINVAL;
+  }
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u)) {
+    msg = "k, v and the pools must be 16-byte aligned, slot_mapping 8-byte aligned";
+    return PA_EINVAL;
+  }
+  WriteFp8Params p{};
+  p.k = static_cast<const uint4*>(k);
+  p.v = static_cast<const uint4*>(v);
+  p.k_pool = static_cast<uint4*>(k_pool);
+  p.v_pool = static_cast<uint4*>(v_pool);
+  p.slots = slot_mapping;
+  p.err = err_flag;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.src_bf16 = src_dtype == PA_BF16 ? 1 : 0;
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = num_kv_heads;
+  p.chunks_per_row = head_dim / 16;
+  p.block_size = block_size;
+  p.num_blocks = num_blocks;
+  const long long total = static_cast<long long>(num_tokens) * num_kv_heads * p.chunks_per_row;
+  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256,
+                                                        std::max(1, device_sm_count()) * 8LL));
+  pa_write_kv_fp8_kernel<<<grid, 256, 0, stream>>>(p);
+  return cuda_status(cudaGetLastError(), "pa_write_kv_fp8 launch", msg);
 }
 
 pa_status run_copy_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,

@@ -67,6 +67,9 @@ def lib() -> ctypes.CDLL:
         L.pa_decode.argtypes = [ctypes.POINTER(pa_decode_args), _vp]
         L.pa_write_kv.restype = ctypes.c_int
         L.pa_write_kv.argtypes = [_vp] * 5 + [_i32] * 5 + [ctypes.c_int, _vp, _vp]
+        L.pa_write_kv_fp8.restype = ctypes.c_int
+        L.pa_write_kv_fp8.argtypes = [_vp, _vp, ctypes.c_int, _vp, _vp, _vp] + [_i32] * 5 + [
+            ctypes.c_float, ctypes.c_float, _vp, _vp]
         L.pa_copy_blocks.restype = ctypes.c_int
         L.pa_copy_blocks.argtypes = [_vp, _vp, _i32, _vp, _i32, _i32, ctypes.c_size_t, _vp, _vp]
         L.pa_swap_blocks.restype = ctypes.c_int
@@ -193,6 +196,21 @@ def pa_write_kv(k: torch.Tensor, v: torch.Tensor, k_pool: torch.Tensor, v_pool: 
     _check(lib().pa_write_kv(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping),
                              t, hkv, d, bsz, nblk, kv_dtype_code(k_pool), _ptr(err_flag),
                              _stream(stream)))
+
+
+def pa_write_kv_fp8(k: torch.Tensor, v: torch.Tensor, k_pool: torch.Tensor,
+                    v_pool: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float,
+                    v_scale: float, *, err_flag: Optional[torch.Tensor] = None,
+                    stream=None) -> None:
+    """f16/bf16 k, v [num_tokens][num_kv_heads][head_dim] quantised into uint8 E4M3 pools."""
+    t, hkv, d = k.shape
+    nblk, _, bsz, _ = k_pool.shape
+    src = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}.get(k.dtype)
+    if src is None or v.dtype != k.dtype:
+        raise PaError(PA_EINVAL, "k and v must both be float16 or both bfloat16")
+    _check(lib().pa_write_kv_fp8(_ptr(k), _ptr(v), src, _ptr(k_pool), _ptr(v_pool),
+                                 _ptr(slot_mapping), t, hkv, d, bsz, nblk, float(k_scale),
+                                 float(v_scale), _ptr(err_flag), _stream(stream)))
 
 
 def _ptr_array(ts: Sequence[torch.Tensor]):

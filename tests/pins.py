@@ -310,9 +310,9 @@ def pin_write_kv(orc):
 
 def pin_write_kv_fp8(orc):
     """Quantise-on-write stores in each new token's slot the library-cast E4M3 code of
-    value / scale (binary32 quotient): the same pools as quantising first and then writing the
-    bytes with the pinned raw write_kv. Specials included: signed zeros, infinities, values
-    beyond 448, f16 subnormals, NaN."""
+    value * (1 / scale) (reciprocal and product in binary32): the same pools as quantising first
+    and then writing the bytes with the pinned raw write_kv. Specials included: signed zeros,
+    infinities, values beyond 448, f16 subnormals, NaN."""
     specials = [0.0, -0.0, math.inf, -math.inf, 1.0e4, -1.0e4, 3.0e-6, math.nan]
     for i, src in enumerate(("bf16", "f16")):
         spec = synth.DecodeSpec(f"q8_{src}", 6, 8, 2, 64, 8, "e4m3", src, ctx_range=(1, 40))
@@ -336,7 +336,7 @@ def pin_write_kv_fp8(orc):
         assert rc == 0
 
         def quant(t, sc):
-            q = t.to(torch.float32).numpy() / np.float32(sc)
+            q = t.to(torch.float32).numpy() * (np.float32(1.0) / np.float32(sc))
             codes = _e4m3_library(q)
             codes[np.isnan(q)] = 0x7F
             return codes

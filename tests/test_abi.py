@@ -23,7 +23,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted([
         "pa_copy_blocks", "pa_decode", "pa_decode_static_workspace", "pa_decode_workspace_size",
-        "pa_last_error_message", "pa_status_string", "pa_swap_blocks", "pa_write_kv"])
+        "pa_last_error_message", "pa_status_string", "pa_swap_blocks", "pa_write_kv",
+        "pa_write_kv_fp8"])
 
 
 def test_library_exports_every_declared_symbol():

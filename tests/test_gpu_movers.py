@@ -1,4 +1,7 @@
-"""pa_write_kv, pa_copy_blocks and pa_swap_blocks on the GPU: bit-exact against the oracle."""
+"""pa_write_kv, pa_write_kv_fp8, pa_copy_blocks and pa_swap_blocks on the GPU: bit-exact against
+the oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -55,6 +58,95 @@ def test_write_kv_out_of_pool_flagged():
     torch.cuda.synchronize()
     assert int(err.item()) & pa.PA_ERR_BLOCK_ID
     assert torch.equal(before.view(torch.uint8), case.k_pool.view(torch.uint8))
+
+
+def _nan_codes_agree(got: np.ndarray, exp: np.ndarray) -> bool:
+    """Equal codes, except that where the oracle wrote its NaN code the kernel may write the
+    NaN code of either sign (the sign of a NaN carries nothing)."""
+    nan = exp == 0x7F
+    return np.array_equal(got[~nan], exp[~nan]) and bool(np.all((got[nan] & 0x7F) == 0x7F))
+
+
+@pytest.mark.parametrize("src", ["bf16", "f16"])
+def test_write_kv_fp8_every_bit_pattern(src):
+    """All 65,536 source bit patterns, over several scales, quantised on write: the pools equal
+    the oracle's, code for code."""
+    orc = oracle.load()
+    dt = torch.bfloat16 if src == "bf16" else torch.float16
+    D, B = 128, 16
+    ntok = 65536 // D
+    vals = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(dt).reshape(ntok, 1, D)
+    perm = torch.randperm(65536, generator=torch.Generator().manual_seed(3))
+    vvals = vals.reshape(-1)[perm].reshape(ntok, 1, D).contiguous()
+    nblk = ntok // B + 2
+    slots = (torch.randperm(nblk * B, generator=torch.Generator().manual_seed(4))[:ntok]
+             .to(torch.int64))
+    for ks, vs in ((1.0, 1.0), (0.05, 0.37), (3.3e-3, 170.0)):
+        kp = torch.full((nblk, 1, B, D), 0xAB, dtype=torch.uint8)
+        vp = torch.full((nblk, 1, B, D), 0xCD, dtype=torch.uint8)
+        exp_k, exp_v = _u8(kp), _u8(vp)
+        assert orc.write_kv_fp8(vals, vvals, exp_k, exp_v, slots, src_dtype=src, num_kv_heads=1,
+                                head_dim=D, block_size=B, k_scale=ks, v_scale=vs) == 0
+        gk, gv = kp.cuda(), vp.cuda()
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pa.pa_write_kv_fp8(vals.cuda(), vvals.cuda(), gk, gv, slots.cuda(), ks, vs, err_flag=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert _nan_codes_agree(_u8(gk), exp_k), (src, ks)
+        assert _nan_codes_agree(_u8(gv), exp_v), (src, vs)
+
+
+def test_write_kv_fp8_then_decode():
+    """A step on an E4M3 cache written by quantise-on-write: bit-exact pools (padding and an
+    out-of-pool slot included), then the decode of the written cache matches the oracle."""
+    orc = oracle.load()
+    spec = synth.SPECS["fp8_long"].scaled(num_seqs=8, ctx_range=(40, 600))
+    case = synth.make_case(spec, seed=77)
+    g = torch.Generator().manual_seed(9)
+    shape = (spec.num_seqs, spec.num_kv_heads, spec.head_dim)
+    k_new = (torch.randn(shape, generator=g) * 2).to(torch.bfloat16)
+    v_new = torch.randn(shape, generator=g).to(torch.bfloat16)
+    ks = float(k_new.float().abs().max()) / 448.0
+    vs = float(v_new.float().abs().max()) / 448.0
+    sm = torch.cat([case.slot_mapping, torch.tensor([-1], dtype=torch.int64)])
+    kn = torch.cat([k_new, k_new[:1]])
+    vn = torch.cat([v_new, v_new[:1]])
+    exp_k, exp_v = _u8(case.k_pool), _u8(case.v_pool)
+    assert orc.write_kv_fp8(kn, vn, exp_k, exp_v, sm, src_dtype="bf16",
+                            num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                            block_size=spec.block_size, k_scale=ks, v_scale=vs) == 0
+    gcase = case.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_write_kv_fp8(kn.cuda(), vn.cuda(), gcase.k_pool, gcase.v_pool, sm.cuda(), ks, vs,
+                       err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(_u8(gcase.k_pool), exp_k) and np.array_equal(_u8(gcase.v_pool), exp_v)
+    # the newest tokens now hold codes of value / (ks, vs); decode the whole cache with those
+    # per-tensor scales on both sides
+    scaled = dataclasses.replace(gcase, k_scale=ks, v_scale=vs)
+    out = gpu_decode(scaled)
+    ref = oracle_decode(scaled)
+    assert max_abs_err(out, ref) <= TOL["e4m3"]
+    bad = torch.tensor([case.num_blocks * spec.block_size], dtype=torch.int64, device="cuda")
+    before = _u8(gcase.k_pool)
+    pa.pa_write_kv_fp8(kn[:1].cuda(), vn[:1].cuda(), gcase.k_pool, gcase.v_pool, bad, ks, vs,
+                       err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_ERR_BLOCK_ID
+    assert np.array_equal(_u8(gcase.k_pool), before)
+
+
+def test_write_kv_fp8_host_validation():
+    k = torch.zeros(2, 1, 128, dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros(4, 1, 16, 128, dtype=torch.uint8, device="cuda")
+    sm = torch.zeros(2, dtype=torch.int64, device="cuda")
+    for ks in (0.0, -1.0, float("inf"), float("nan")):
+        with pytest.raises(pa.PaError) as e:
+            pa.pa_write_kv_fp8(k, k, pool, pool, sm, ks, 1.0)
+        assert e.value.status == pa.PA_EINVAL
+    with pytest.raises(pa.PaError):
+        pa.pa_write_kv_fp8(k.float(), k.float(), pool, pool, sm, 1.0, 1.0)
 
 
 @pytest.mark.parametrize("layers,block_bytes_kib", [(1, 32), (3, 2), (4, 64)])

@@ -63,8 +63,8 @@ MUTANTS = [
     ("encode_subnormal_step", "round_half_even(ldexp(a, 9))", "round_half_even(ldexp(a, 8))", 1),
     ("encode_sign_dropped", "return sign | (uint8_t)(((E + 7) << 3) | q);",
      "return (uint8_t)(((E + 7) << 3) | q);", 1),
-    ("quantise_multiplies", "/ (double)k_scale", "* (double)k_scale", 1),
-    ("quantise_v_with_k_scale", "/ (double)v_scale", "/ (double)k_scale", 1),
+    ("quantise_by_scale_not_inverse", "* (double)k_inv", "* (double)k_scale", 1),
+    ("quantise_v_with_k_inverse", "* (double)v_inv", "* (double)k_inv", 1),
 ]
 
 
