@@ -53,7 +53,8 @@ typedef enum {
   PA_OK = 0,
   PA_EINVAL = 1,        /* invalid argument; nothing was enqueued */
   PA_EUNSUPPORTED = 2,  /* valid but not built: dtype / head_dim / group combination */
-  PA_ECUDA = 3          /* a CUDA runtime call or launch failed */
+  PA_ECUDA = 3,         /* a CUDA runtime call or launch failed */
+  PA_ENOSPACE = 4       /* a host-side pool ran out (a scheduler's CPU swap slots) */
 } pa_status;
 
 typedef enum {

@@ -33,6 +33,8 @@ const char* pa_status_string(pa_status status) {
       return "PA_EUNSUPPORTED: combination not built";
     case PA_ECUDA:
       return "PA_ECUDA: CUDA runtime error";
+    case PA_ENOSPACE:
+      return "PA_ENOSPACE: host-side pool exhausted";
   }
   return "unknown pa_status";
 }

@@ -15,7 +15,7 @@ import torch
 
 from . import build as _build
 
-PA_OK, PA_EINVAL, PA_EUNSUPPORTED, PA_ECUDA = 0, 1, 2, 3
+PA_OK, PA_EINVAL, PA_EUNSUPPORTED, PA_ECUDA, PA_ENOSPACE = 0, 1, 2, 3, 4
 PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 PA_SWAP_OUT, PA_SWAP_IN = 0, 1
 PA_ERR_BLOCK_ID, PA_ERR_CTX_LEN, PA_ERR_TIMEOUT = 1, 2, 4

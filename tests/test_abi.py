@@ -1,6 +1,7 @@
 """The C-ABI library without a GPU: it builds for sm_103a, loads, exports every entry point the
 header declares, matches the binding's struct layout and validates arguments on the host."""
 import ctypes
+import glob
 import os
 import re
 import subprocess
@@ -12,19 +13,25 @@ from paged_kv_cache_38_gb300 import build as pa_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "pa.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
-def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+def declared_functions(header=None):
+    names = set()
+    for path in [header] if header else HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+        names.update(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
-    assert declared_functions() == sorted([
+    assert declared_functions(HEADER) == sorted([
         "pa_copy_blocks", "pa_decode", "pa_decode_static_workspace", "pa_decode_workspace_size",
         "pa_last_error_message", "pa_status_string", "pa_swap_blocks", "pa_write_kv",
         "pa_write_kv_fp8"])
+    assert declared_functions(os.path.join(os.path.dirname(HEADER), "pa_scheduler.h")) == sorted([
+        "pa_scheduler_add_request", "pa_scheduler_create", "pa_scheduler_destroy",
+        "pa_scheduler_free_blocks", "pa_scheduler_has_unfinished", "pa_scheduler_step"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -37,12 +44,17 @@ def test_library_exports_every_declared_symbol():
         assert hasattr(lib, name)
 
 
-def test_struct_layout_matches_header(tmp_path):
-    fields = [f for f, _ in pa.pa.pa_decode_args._fields_]
+@pytest.mark.parametrize("name,header,cls", [
+    ("pa_decode_args", "pa.h", lambda: pa.pa.pa_decode_args),
+    ("pa_step_plan", "pa_scheduler.h", lambda: __import__(
+        "paged_kv_cache_38_gb300.scheduler", fromlist=["x"]).pa_step_plan)])
+def test_struct_layout_matches_header(tmp_path, name, header, cls):
+    struct = cls()
+    fields = [f for f, _ in struct._fields_]
     src = tmp_path / "layout.c"
-    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "pa.h"', 'int main(void){',
-             'printf("%zu\\n", sizeof(pa_decode_args));']
-    lines += [f'printf("%zu\\n", offsetof(pa_decode_args, {f}));' for f in fields]
+    lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{header}"', 'int main(void){',
+             f'printf("%zu\\n", sizeof({name}));']
+    lines += [f'printf("%zu\\n", offsetof({name}, {f}));' for f in fields]
     lines += ["return 0;}"]
     src.write_text("\n".join(lines))
     exe = tmp_path / "layout"
@@ -50,14 +62,14 @@ def test_struct_layout_matches_header(tmp_path):
                     str(exe)], check=True)
     vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
                                            check=True).stdout.split()]
-    assert vals[0] == ctypes.sizeof(pa.pa.pa_decode_args)
+    assert vals[0] == ctypes.sizeof(struct)
     for f, off in zip(fields, vals[1:]):
-        assert getattr(pa.pa.pa_decode_args, f).offset == off, f
+        assert getattr(struct, f).offset == off, f
 
 
 def test_status_strings():
     lib = pa.lib()
-    for code in (pa.PA_OK, pa.PA_EINVAL, pa.PA_EUNSUPPORTED, pa.PA_ECUDA):
+    for code in (pa.PA_OK, pa.PA_EINVAL, pa.PA_EUNSUPPORTED, pa.PA_ECUDA, pa.pa.PA_ENOSPACE):
         assert lib.pa_status_string(code).startswith(b"PA_")
 
 
