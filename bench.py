@@ -450,6 +450,77 @@ def run_extras(args, dev, flush, peaks) -> dict:
     res["preemption_swap"] = run_swap_bench(dev)
     res["copy_blocks_large"] = run_copy_bench(dev, flush, peaks)
     res["write_kv_fp8"] = run_quantise_bench(dev, flush, peaks)
+    res["scheduler"] = run_scheduler_bench(dev)
+    return res
+
+
+def run_scheduler_bench(dev) -> dict:
+    """The C++ scheduler driving the kernels: the GQA workload's geometry (32 q / 8 kv heads x
+    128, bf16, 16-token blocks) with 25 groups of 4 samples sharing a 512-token prompt plus 60
+    single requests, in a pool of 12,000 blocks. Reports the host time of one scheduling step
+    and the served loop (plan, moves, KV writes, decode) over 150 steps, eager."""
+    import paged_kv_cache_38_gb300 as pa
+    from paged_kv_cache_38_gb300 import scheduler as sch
+
+    hq, hkv, d, b, nblk = 32, 8, 128, 16, 12000
+    rng = np.random.default_rng(SEED)
+
+    def requests(s):
+        for r in range(25):
+            s.add_request(r, 512 + int(rng.integers(1, 64)), 400, 4)
+        for r in range(25, 85):
+            s.add_request(r, int(rng.integers(256, 2048)), 400, 1)
+
+    s = sch.Scheduler(nblk, b, 512, 256, sch.SWAP, 4 * nblk)
+    requests(s)
+    host = []
+    for _ in range(150):
+        t0 = time.perf_counter()
+        s.step()
+        host.append(time.perf_counter() - t0)
+    # the served loop on the GPU
+    s = sch.Scheduler(nblk, b, 512, 256, sch.SWAP, 4 * nblk)
+    rng = np.random.default_rng(SEED)
+    requests(s)
+    g = torch.Generator(device=dev).manual_seed(SEED)
+    rows = 4096
+    k_rows = torch.randn(rows, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    v_rows = torch.randn(rows, hkv, d, generator=g, device=dev).to(torch.bfloat16)
+    kp = torch.empty(nblk, hkv, b, d, dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    cpu_pool = torch.empty(1, 1, 2, hkv * b * d * 2, dtype=torch.uint8).pin_memory()
+    q_all = torch.randn(512, hq, d, generator=g, device=dev).to(torch.bfloat16)
+    ws = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    tokens, writes, steps = 0, 0, 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(150):
+        plan = s.step()
+        if len(plan.swap_out_np) or len(plan.swap_in_np):
+            raise RuntimeError("the served-loop workload is sized to run without swapping")
+        sch.execute_moves(plan, [kp], [vp], cpu_pool)
+        if len(plan.slots_np):
+            idx = torch.from_numpy(plan.slots_np % rows).to(dev, non_blocking=True)
+            pa.pa_write_kv(k_rows[idx], v_rows[idx], kp, vp,
+                           torch.from_numpy(plan.slots_np).to(dev, non_blocking=True))
+        n = len(plan.seq_ids_np)
+        if n:
+            bt = torch.from_numpy(plan.tables_np).to(dev, non_blocking=True)
+            cl = torch.from_numpy(plan.ctx_np).to(dev, non_blocking=True)
+            pa.pa_decode(q_all[:n], kp, vp, bt, cl, d ** -0.5, max_ctx_len=int(plan.ctx_np.max()),
+                         workspace=ws)
+        tokens += n
+        writes += len(plan.slots_np)
+        steps += 1
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    res = {"requests": 85, "sequences": 160, "pool_blocks": nblk,
+           "host_step_us_median": round(1e6 * statistics.median(host), 1),
+           "served_steps": steps, "served_ms_per_step": round(1e3 * wall / steps, 3),
+           "served_decode_tokens_per_s": round(tokens / wall, 1),
+           "kv_positions_written": writes}
+    del kp, vp, ws
+    torch.cuda.empty_cache()
     return res
 
 

@@ -261,12 +261,16 @@ struct pa_scheduler {
 
     // 5. the batch
     std::unordered_map<const Seq*, int32_t> index;
+    const int64_t n = running_seqs();
+    tables.resize(static_cast<size_t>(n) * max_blocks);
+    int32_t* row = tables.data();
     for (const Group* g : running)
       for (const Seq& s : g->seqs) {
         index[&s] = static_cast<int32_t>(seq_ids.size());
         seq_ids.push_back(g->id * 256 + s.sample);
-        for (int32_t j = 0; j < max_blocks; ++j)
-          tables.push_back(j < static_cast<int32_t>(s.table.size()) ? s.table[j] : -1);
+        std::copy(s.table.begin(), s.table.end(), row);
+        std::fill(row + s.table.size(), row + max_blocks, -1);
+        row += max_blocks;
         ctx_lens.push_back(s.length);
       }
     for (const Write& w : writes) {

@@ -1,13 +1,12 @@
 """ctypes binding of ``include/pa_scheduler.h`` (argument marshalling only).
 
-``Scheduler`` wraps one ``pa_scheduler``; ``step()`` copies the C plan into a ``Plan`` holding
-Python lists (for checks) and numpy arrays (for the kernels: block tables, context lengths,
-slot mapping, copy pairs, swap lists).
+``Scheduler`` wraps one ``pa_scheduler``; ``step()`` copies the C plan into a ``Plan`` of numpy
+arrays (for the kernels: block tables, context lengths, slot mapping, copy pairs, swap lists),
+with list views of the same data for checks.
 """
 from __future__ import annotations
 
 import ctypes
-from dataclasses import dataclass
 from typing import List, Tuple
 
 import numpy as np
@@ -56,27 +55,57 @@ def _arr(ptr, n, dtype) -> np.ndarray:
     return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dtype, copy=True)
 
 
-@dataclass
 class Plan:
-    seq_ids: List[int]
-    block_tables: List[List[int]]
-    ctx_lens: List[int]
-    writes: List[Tuple[int, int, int]]
-    copies: List[Tuple[int, int]]
-    swap_out: List[Tuple[int, int]]
-    swap_in: List[Tuple[int, int]]
-    finished: List[int]
-    preempted: List[int]
-    num_free_blocks: int
-    # the same data as arrays
-    tables_np: np.ndarray     # int32 [num_seqs][max_blocks_per_seq]
-    ctx_np: np.ndarray        # int32 [num_seqs]
-    write_seq_np: np.ndarray  # int32 [num_writes]
-    write_pos_np: np.ndarray  # int32 [num_writes]
-    slots_np: np.ndarray      # int64 [num_writes]
-    copies_np: np.ndarray     # int32 [num_copies][2]
-    swap_out_np: np.ndarray   # int32 [n][2] (GPU block, CPU slot)
-    swap_in_np: np.ndarray    # int32 [n][2] (CPU slot, GPU block)
+    """One step's plan as arrays (copies of the scheduler's, so they outlive its next step);
+    the list views of the same data are built on first use."""
+
+    def __init__(self, seq_ids, tables, ctx, write_seq, write_pos, slots, copies, swap_out,
+                 swap_in, finished, preempted, num_free_blocks):
+        self.seq_ids_np = seq_ids     # int64 [num_seqs]
+        self.tables_np = tables       # int32 [num_seqs][max_blocks_per_seq]
+        self.ctx_np = ctx             # int32 [num_seqs]
+        self.write_seq_np = write_seq  # int32 [num_writes]
+        self.write_pos_np = write_pos  # int32 [num_writes]
+        self.slots_np = slots         # int64 [num_writes]
+        self.copies_np = copies       # int32 [num_copies][2] (src, dst)
+        self.swap_out_np = swap_out   # int32 [n][2] (GPU block, CPU slot)
+        self.swap_in_np = swap_in     # int32 [n][2] (CPU slot, GPU block)
+        self.finished: List[int] = finished
+        self.preempted: List[int] = preempted
+        self.num_free_blocks = num_free_blocks
+
+    @staticmethod
+    def _pairs(a: np.ndarray) -> List[Tuple[int, int]]:
+        return [(int(x), int(y)) for x, y in a]
+
+    @property
+    def seq_ids(self) -> List[int]:
+        return self.seq_ids_np.tolist()
+
+    @property
+    def block_tables(self) -> List[List[int]]:
+        return self.tables_np.tolist()
+
+    @property
+    def ctx_lens(self) -> List[int]:
+        return self.ctx_np.tolist()
+
+    @property
+    def writes(self) -> List[Tuple[int, int, int]]:
+        return list(zip(self.write_seq_np.tolist(), self.write_pos_np.tolist(),
+                        self.slots_np.tolist()))
+
+    @property
+    def copies(self) -> List[Tuple[int, int]]:
+        return self._pairs(self.copies_np)
+
+    @property
+    def swap_out(self) -> List[Tuple[int, int]]:
+        return self._pairs(self.swap_out_np)
+
+    @property
+    def swap_in(self) -> List[Tuple[int, int]]:
+        return self._pairs(self.swap_in_np)
 
 
 class Scheduler:
@@ -107,24 +136,15 @@ class Scheduler:
         if st != 0:
             raise PaError(st, self._lib.pa_last_error_message().decode())
         n, mb = p.num_seqs, self.max_blocks
-        tables = _arr(p.block_tables, n * mb, np.int32).reshape(n, mb)
-        ctx = _arr(p.ctx_lens, n, np.int32)
-        ws, wp = _arr(p.write_seq, p.num_writes, np.int32), _arr(p.write_pos, p.num_writes, np.int32)
-        slots = _arr(p.slot_mapping, p.num_writes, np.int64)
-        copies = _arr(p.copies, 2 * p.num_copies, np.int32).reshape(-1, 2)
-        sout = _arr(p.swap_out, 2 * p.num_swap_out, np.int32).reshape(-1, 2)
-        sin = _arr(p.swap_in, 2 * p.num_swap_in, np.int32).reshape(-1, 2)
-        pairs = lambda a: [tuple(int(v) for v in r) for r in a]  # noqa: E731
         return Plan(
-            seq_ids=_arr(p.seq_ids, n, np.int64).tolist(), block_tables=tables.tolist(),
-            ctx_lens=ctx.tolist(),
-            writes=[(int(a), int(b), int(c)) for a, b, c in zip(ws, wp, slots)],
-            copies=pairs(copies), swap_out=pairs(sout), swap_in=pairs(sin),
-            finished=_arr(p.finished, p.num_finished, np.int64).tolist(),
-            preempted=_arr(p.preempted, p.num_preempted, np.int64).tolist(),
-            num_free_blocks=int(p.num_free_blocks), tables_np=tables, ctx_np=ctx,
-            write_seq_np=ws, write_pos_np=wp, slots_np=slots, copies_np=copies,
-            swap_out_np=sout, swap_in_np=sin)
+            _arr(p.seq_ids, n, np.int64), _arr(p.block_tables, n * mb, np.int32).reshape(n, mb),
+            _arr(p.ctx_lens, n, np.int32), _arr(p.write_seq, p.num_writes, np.int32),
+            _arr(p.write_pos, p.num_writes, np.int32), _arr(p.slot_mapping, p.num_writes, np.int64),
+            _arr(p.copies, 2 * p.num_copies, np.int32).reshape(-1, 2),
+            _arr(p.swap_out, 2 * p.num_swap_out, np.int32).reshape(-1, 2),
+            _arr(p.swap_in, 2 * p.num_swap_in, np.int32).reshape(-1, 2),
+            _arr(p.finished, p.num_finished, np.int64).tolist(),
+            _arr(p.preempted, p.num_preempted, np.int64).tolist(), int(p.num_free_blocks))
 
     @property
     def free(self) -> List[int]:
@@ -138,3 +158,32 @@ class Scheduler:
 
     def has_unfinished(self) -> bool:
         return bool(self._lib.pa_scheduler_has_unfinished(self._h))
+
+
+def execute_moves(plan: Plan, k_pools, v_pools, cpu_pool, *, err_flag=None, stream=None) -> None:
+    """Enqueue a plan's block moves in the order the plan requires: swap-outs (GPU block ->
+    CPU slot), swap-ins (CPU slot -> GPU block), then copy-on-write copies. ``cpu_pool`` is a
+    pinned uint8 tensor [num_cpu_blocks][layers][2][block_bytes]; runs of consecutive CPU slots
+    move in one call. The KV writes and the decode are the caller's (they need the new K/V)."""
+    import torch
+
+    from .pa import PA_SWAP_IN, PA_SWAP_OUT, pa_copy_blocks, pa_swap_blocks
+
+    def runs(pairs, slot_col):
+        i = 0
+        while i < len(pairs):
+            j = i + 1
+            while j < len(pairs) and pairs[j][slot_col] == pairs[j - 1][slot_col] + 1:
+                j += 1
+            yield pairs[i][slot_col], [p[1 - slot_col] for p in pairs[i:j]]
+            i = j
+
+    for c0, blocks in runs(plan.swap_out, 1) if len(plan.swap_out_np) else ():
+        pa_swap_blocks(k_pools, v_pools, cpu_pool[c0:c0 + len(blocks)], blocks, PA_SWAP_OUT,
+                       stream=stream)
+    for c0, blocks in runs(plan.swap_in, 0) if len(plan.swap_in_np) else ():
+        pa_swap_blocks(k_pools, v_pools, cpu_pool[c0:c0 + len(blocks)], blocks, PA_SWAP_IN,
+                       stream=stream)
+    if len(plan.copies_np):
+        pairs = torch.from_numpy(plan.copies_np).to(k_pools[0].device, non_blocking=False)
+        pa_copy_blocks(k_pools, v_pools, pairs, err_flag=err_flag, stream=stream)
