@@ -451,7 +451,65 @@ def run_extras(args, dev, flush, peaks) -> dict:
     res["copy_blocks_large"] = run_copy_bench(dev, flush, peaks)
     res["write_kv_fp8"] = run_quantise_bench(dev, flush, peaks)
     res["scheduler"] = run_scheduler_bench(dev)
+    res["block_size_sweep"] = run_block_sweep(dev, flush, peaks)
     return res
+
+
+def run_block_sweep(dev, flush, peaks) -> dict:
+    """Block sizes 8, 16, 32, 64 (the summary page's ablation: decode cost and swap bandwidth
+    against block size). Decode: the GQA workload rebuilt at each block size (same contexts and
+    512-token shared prompts). Swap: the preemption victim's 1,500 tokens over 32 layers of
+    8 kv heads x 128 bf16, out and back, direct (mapped pinned memory) and staged (one copy)."""
+    import paged_kv_cache_38_gb300 as pa
+
+    out = {}
+    for B in (8, 16, 32, 64):
+        spec = synth.SPECS["gqa_pressure"].scaled(name=f"gqa_pressure_b{B}", block_size=B)
+        case = synth.make_case(spec, seed=SEED, device=dev, logical=False, poison=False)
+        split = split_tokens_for(spec)
+        st = Step(case, split)
+        for _ in range(3):
+            st.decode()
+        t = statistics.mean(time_steps(st.decode, 10, flush))
+        byts = decode_bytes(case, split)["total"]
+        row = {"decode_us": round(t * 1e3, 1), "decode_gbs": round(byts / (t * 1e-3) / 1e9, 1),
+               "decode_pct_of_peak": round(100 * byts / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 1)}
+        del case, st
+        torch.cuda.empty_cache()
+        # swap of one 1,500-token sequence over 32 layers
+        layers, hkv, d = 32, 8, 128
+        n = -(-1500 // B)
+        nblk = 2 * n + 8
+        kp = [torch.empty(nblk, hkv, B, d, dtype=torch.bfloat16, device=dev) for _ in range(layers)]
+        vp = [torch.empty_like(kp[0]) for _ in range(layers)]
+        perm = np.random.default_rng(SEED + B).permutation(nblk).astype(np.int32)
+        out_ids, in_ids = perm[:n], perm[n:2 * n]
+        bb = hkv * B * d * 2
+        total = n * layers * 2 * bb
+        host = torch.empty(total, dtype=torch.uint8).pin_memory()
+        staging = torch.empty(total, dtype=torch.uint8, device=dev)
+        for mode, stg in (("direct", None), ("staged", staging)):
+            ts_o, ts_i = [], []
+            for _ in range(5):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                pa.pa_swap_blocks(kp, vp, host, out_ids, pa.PA_SWAP_OUT, staging=stg)
+                b.record()
+                b.synchronize()
+                ts_o.append(a.elapsed_time(b))
+                a.record()
+                pa.pa_swap_blocks(kp, vp, host, in_ids, pa.PA_SWAP_IN, staging=stg)
+                b.record()
+                b.synchronize()
+                ts_i.append(a.elapsed_time(b))
+            row[f"swap_{mode}_out_gbs"] = round(total / (min(ts_o) * 1e-3) / 1e9, 1)
+            row[f"swap_{mode}_in_gbs"] = round(total / (min(ts_i) * 1e-3) / 1e9, 1)
+        row["swap_bytes_each_way"] = total
+        row["swap_blocks"] = n
+        out[f"b{B}"] = row
+        del kp, vp, host, staging
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_scheduler_bench(dev) -> dict:

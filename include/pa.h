@@ -97,7 +97,7 @@ typedef enum {
  *   ctx_lens     [num_seqs]                                  int32
  *   out          [num_seqs][num_q_heads][head_dim]           q_dtype
  *   workspace    >= pa_decode_workspace_size(args) bytes, 256-byte aligned, contents ignored
- * Supported: head_dim in {64, 128}; block_size in {4, 8, 16, 32}; group size
+ * Supported: head_dim in {64, 128}; block_size in {4, 8, 16, 32, 64}; group size
  * num_q_heads/num_kv_heads in {1, 2, 4, 8, 16}; (q, kv) dtype pairs (F16, F16), (BF16, BF16),
  * (F16, FP8_E4M3), (BF16, FP8_E4M3). k_scale / v_scale multiply the stored values (use 1.0
  * for 16-bit KV). Work is split along the context ("split-K") when that improves occupancy;

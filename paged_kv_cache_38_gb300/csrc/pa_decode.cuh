@@ -47,7 +47,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = 32 * (1 + kProducerWarps + kConsumerWarps);
 constexpr int kMaxStages = 32;
 constexpr int kItemSlots = 2;          // work items queued ahead by the scheduler warp
-constexpr int kMaxItemBlocks = 256;    // block-table entries of one work item
+constexpr int kMaxItemUnits = 256;     // copy units (table rows) of one work item
 constexpr int kMaxSeqsPerLaunch = 4096;
 constexpr int kScanWarps = kDecodeThreads / 32;
 constexpr int kRemBuckets = 32;  // size classes of the last-split items (longest first)
@@ -70,12 +70,13 @@ struct DecodeParams {
   int32_t* err;
   int num_seqs, num_q_heads, num_kv_heads;
   int block_size, log2_block, num_blocks, max_blocks, max_ctx;
+  int log2_srows;       // log2 of the rows per (block, kv head) copy: min(block_size, stage_tokens)
   int split_tokens;     // tokens per work item, a multiple of max(16, block_size)
   int max_splits;       // ceil(max_ctx / split_tokens)
   int stages;           // shared-memory ring depth, a multiple of kConsumerWarps
-  int region_stride;    // bytes of one 128-byte-wide column region of one block in a stage
+  int region_stride;    // bytes of one 128-byte-wide column region of one copy in a stage
   int stage_bytes;      // bytes of K (or V) in one stage
-  int stage_tokens;     // tokens per stage: a multiple of 16, at most 4 blocks
+  int stage_tokens;     // tokens per stage: a multiple of 16; at most 4 blocks, or part of one
   // byte offsets from the 1024-aligned shared-memory base
   int off_merge, off_q, off_bar, off_meta, off_items, off_tbl, off_scan;
   int tbl_stride;       // block-table entries per item slot
@@ -93,7 +94,8 @@ struct ItemDesc {
   int ntiles;   // ring stages of this item
   int tok0;     // first token of the item
   int tok_end;  // one past its last token
-  int nblk;     // blocks of the item (their physical ids, or -1, follow in the table slot)
+  int nunits;   // copy units of the item: srows rows of one (block, kv head) tile each; their
+                // tensor-map row coordinates (or -1 for a block outside the pool) fill the slot
 };
 
 template <int KV, int D>
@@ -199,7 +201,7 @@ struct Consumer<KV, D, G, false> {
 #pragma unroll
     for (int it = 0; it < kIters; ++it) {
       const int r = it * kGroups + grp;
-      const StageRow row = stage_row(r0 + r, p.log2_block, Gm::kRegions, p.region_stride);
+      const StageRow row = stage_row(r0 + r, p.log2_srows, Gm::kRegions, p.region_stride);
       float k[kE];
       load_row(chunk_addr(ks, row, ci, p.region_stride), k);
 #pragma unroll
@@ -232,7 +234,7 @@ struct Consumer<KV, D, G, false> {
     for (int it = 0; it < kIters; ++it) {
       const int r = it * kGroups + grp;
       if (!((valid >> r) & 1u)) continue;
-      const StageRow row = stage_row(r0 + r, p.log2_block, Gm::kRegions, p.region_stride);
+      const StageRow row = stage_row(r0 + r, p.log2_srows, Gm::kRegions, p.region_stride);
       float v[kE];
       load_row(chunk_addr(vs, row, ci, p.region_stride), v);
 #pragma unroll
@@ -353,7 +355,7 @@ struct Consumer<KV, D, G, true> {
       uint32_t ka[2][16];
 #pragma unroll
       for (int hi = 0; hi < 2; ++hi) {
-        const StageRow row = stage_row(r0 + g + 8 * hi, p.log2_block, Gm::kRegions, p.region_stride);
+        const StageRow row = stage_row(r0 + g + 8 * hi, p.log2_srows, Gm::kRegions, p.region_stride);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const uint4 v = lds128(chunk_addr(ks, row, 2 * t4 + cc, p.region_stride));
@@ -375,7 +377,7 @@ struct Consumer<KV, D, G, true> {
     } else {
       const int i = lane >> 3;
       const StageRow row =
-          stage_row(r0 + (lane & 7) + 8 * (i & 1), p.log2_block, Gm::kRegions, p.region_stride);
+          stage_row(r0 + (lane & 7) + 8 * (i & 1), p.log2_srows, Gm::kRegions, p.region_stride);
 #pragma unroll
       for (int j = 0; j < kK; ++j) {
         uint32_t a0, a1, a2, a3;
@@ -446,8 +448,8 @@ struct Consumer<KV, D, G, true> {
       uint32_t va[2][16];
 #pragma unroll
       for (int pair = 0; pair < 2; ++pair) {
-        const StageRow ra = stage_row(r0 + 2 * t4 + 8 * pair, p.log2_block, Gm::kRegions, p.region_stride);
-        const StageRow rb = stage_row(r0 + 2 * t4 + 8 * pair + 1, p.log2_block, Gm::kRegions, p.region_stride);
+        const StageRow ra = stage_row(r0 + 2 * t4 + 8 * pair, p.log2_srows, Gm::kRegions, p.region_stride);
+        const StageRow rb = stage_row(r0 + 2 * t4 + 8 * pair + 1, p.log2_srows, Gm::kRegions, p.region_stride);
         const uint4 x = lds128(chunk_addr(vs, ra, g, p.region_stride));
         const uint4 y = lds128(chunk_addr(vs, rb, g, p.region_stride));
         const uint32_t xa[4] = {x.x, x.y, x.z, x.w};
@@ -473,7 +475,7 @@ struct Consumer<KV, D, G, true> {
     } else {
       const int i = lane >> 3;
       const StageRow row =
-          stage_row(r0 + (lane & 7) + 8 * (i >> 1), p.log2_block, Gm::kRegions, p.region_stride);
+          stage_row(r0 + (lane & 7) + 8 * (i >> 1), p.log2_srows, Gm::kRegions, p.region_stride);
 #pragma unroll
       for (int j = 0; j < kK; ++j) {
         uint32_t a0, a1, a2, a3;
@@ -669,8 +671,8 @@ __device__ void combine_heads(const DecodeParams& p, int ns, size_t head0, int l
   }
 }
 
-__device__ __forceinline__ int phs_of(const int (&phs)[4], int b) {
-  return b == 0 ? phs[0] : b == 1 ? phs[1] : b == 2 ? phs[2] : phs[3];
+__device__ __forceinline__ int row_of(const int (&rows)[4], int b) {
+  return b == 0 ? rows[0] : b == 1 ? rows[1] : b == 2 ? rows[2] : rows[3];
 }
 
 template <int KV, int D, int G>
@@ -882,17 +884,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         split = nfull;
       }
       const int tok0 = split * S, tok_end = min(L, tok0 + S);
+      // the row of every copy unit (srows rows of one block's tile for kv head kvh), so the
+      // producers only look it up: unit u starts at token tok0 + u * srows
       const int blk0 = tok0 >> p.log2_block;
-      const int nblk = ((tok_end - 1) >> p.log2_block) - blk0 + 1;
+      const int nunits = (tok_end - tok0 + (1 << p.log2_srows) - 1) >> p.log2_srows;
       const int32_t* trow = p.block_tables + static_cast<size_t>(seq) * p.max_blocks + blk0;
       int* slot_tbl = tbl + slot * p.tbl_stride;
-      for (int j = lane; j < nblk; j += 32) {
-        int ph = __ldg(trow + j);
+      for (int u = lane; u < nunits; u += 32) {
+        const int rel = u << p.log2_srows;
+        int ph = __ldg(trow + (rel >> p.log2_block));
         if (ph < 0 || ph >= p.num_blocks) {
           flag_error(p.err, kErrBlockId);
-          ph = -1;
+          slot_tbl[u] = -1;
+        } else {
+          slot_tbl[u] = (ph * Hkv + kvh) * B + (rel & (B - 1));
         }
-        slot_tbl[j] = ph;
       }
       __syncwarp();
       if (lane == 0) {
@@ -903,7 +909,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         d.ntiles = (tok_end - tok0 + st_tokens - 1) / st_tokens;
         d.tok0 = tok0;
         d.tok_end = tok_end;
-        d.nblk = nblk;
+        d.nunits = nunits;
         // descriptor and table for the producers now, the queries for the consumers on landing
         mbar_arrive(smem_addr(qfull + slot));
         const uint32_t ql = smem_addr(qland + slot);
@@ -927,8 +933,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
     }
-    const uint32_t tile_bytes = static_cast<uint32_t>(2 * Gm::kRegions * B * 128);
-    const int bps = st_tokens >> p.log2_block;  // blocks per stage (1, 2 or 4)
+    // A stage holds bps copies of srows rows each: whole blocks when blocks are at most a stage
+    // (bps = 1, 2 or 4), else one part of one block (bps = 1, srows = stage tokens).
+    const int srows = 1 << p.log2_srows;
+    const uint32_t tile_bytes = static_cast<uint32_t>(2 * Gm::kRegions * srows * 128);
+    const int bps = st_tokens >> p.log2_srows;
     uint32_t g0 = 0;                            // CTA tile index of the item's first tile
     bool ok = true;
     uint32_t issued_last = 0, any = 0;
@@ -955,18 +964,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           break;
         }
         uint32_t valid = 0, bytes = 0;
-        int phs[4];
+        int rows[4];
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-          phs[b] = -1;
-          const int j = t * bps + b;
-          if (b < bps && j < d.nblk) {
-            const int ph = slot_tbl[j];
-            if (ph >= 0) {
-              phs[b] = ph;
+          rows[b] = -1;
+          const int u = t * bps + b;  // copy unit b of stage t
+          if (b < bps && u < d.nunits) {
+            const int row = slot_tbl[u];
+            if (row >= 0) {
+              rows[b] = row;
               bytes += tile_bytes;
-              const int r0 = b * B;
-              const int n = min(B, d.tok_end - (d.tok0 + t * st_tokens + r0));
+              const int r0 = b * srows;
+              const int n = min(srows, d.tok_end - (d.tok0 + t * st_tokens + r0));
               valid |= (n >= 32 ? 0xffffffffu : ((1u << n) - 1u)) << r0;
             }
           }
@@ -980,11 +989,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         {  // one lane per copy: (block b, K|V, column region c)
           constexpr int kOps = 2 * Gm::kRegions;
           const int b = lane / kOps, kv = (lane / Gm::kRegions) & 1, c = lane % Gm::kRegions;
-          if (b < bps && phs_of(phs, b) >= 0) {
+          if (b < bps && row_of(rows, b) >= 0) {
             const uint32_t off = static_cast<uint32_t>(2 * s * p.stage_bytes + kv * p.stage_bytes +
                                                        (b * Gm::kRegions + c) * p.region_stride);
-            tma_load_2d(base + off, kv ? &vmap : &kmap, c * Gm::kColsPerRegion,
-                        (phs_of(phs, b) * Hkv + d.kvh) * B, fb, pol);
+            tma_load_2d(base + off, kv ? &vmap : &kmap, c * Gm::kColsPerRegion, row_of(rows, b),
+                        fb, pol);
           }
         }
         issued_last = g;

@@ -34,9 +34,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // The pool as a 2-D tensor [num_blocks*num_kv_heads*block_size rows][head_dim] with a box of
-// one (block, kv head) tile: block_size rows x 128 bytes, 128-byte swizzle.
+// one copy: `rows` token rows of one (block, kv head) tile x 128 bytes, 128-byte swizzle.
 pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_decode_args& a, int elt,
-                          std::string& msg) {
+                          int box_rows, std::string& msg) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) {
     msg = "cuTensorMapEncodeTiled is not available from the driver";
@@ -45,7 +45,7 @@ pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_decode_ar
   const cuuint64_t rows = static_cast<cuuint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.head_dim), rows};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.head_dim) * elt};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(a.block_size)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                    2, const_cast<void*>(pool), dims, strides, box, estr,
@@ -88,8 +88,9 @@ pa_status check_decode_args(const pa_decode_args& a, bool check_pointers, std::s
     return PA_EINVAL;
   }
   const int group = a.num_q_heads / a.num_kv_heads;
-  if (a.block_size != 4 && a.block_size != 8 && a.block_size != 16 && a.block_size != 32) {
-    msg = "block_size must be 4, 8, 16 or 32";
+  if (a.block_size != 4 && a.block_size != 8 && a.block_size != 16 && a.block_size != 32 &&
+      a.block_size != 64) {
+    msg = "block_size must be 4, 8, 16, 32 or 64";
     return PA_EINVAL;
   }
   if (a.head_dim != 64 && a.head_dim != 128) {
@@ -159,10 +160,12 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   pl.elt = a.kv_dtype == PA_FP8_E4M3 ? 1 : 2;
   pl.regions = D * pl.elt / 128;
   // 16 tokens per stage (32 for 1-byte KV, so a stage still moves 8 KiB per head pair of
-  // K and V and the per-stage costs are paid half as often), at most 4 blocks per stage.
-  pl.stage_tokens = std::max(B, std::min(pl.elt == 1 ? 32 : 16, 4 * B));
-  pl.region_stride = std::max(B * 128, 1024);
-  pl.stage_bytes = (pl.stage_tokens / B) * pl.regions * pl.region_stride;
+  // K and V and the per-stage costs are paid half as often): up to 4 whole blocks when blocks
+  // are smaller, one part of one block when they are larger. Each copy brings srows rows.
+  pl.stage_tokens = std::min(pl.elt == 1 ? 32 : 16, 4 * B);
+  pl.stage_rows = std::min(B, pl.stage_tokens);
+  pl.region_stride = std::max(pl.stage_rows * 128, 1024);
+  pl.stage_bytes = (pl.stage_tokens / pl.stage_rows) * pl.regions * pl.region_stride;
 
   const int stok = std::max(16, B);  // split granularity of the API
   if (a.split_tokens > 0) {
@@ -185,9 +188,9 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
   pl.seqs_per_launch = std::max(1, std::min(a.num_seqs, kMaxSeqsPerLaunch));
 
   // shared memory: [ring][merge][queries][barriers][stage meta][items + flag][tables][scan]
-  const int tbl_entries = pl.split_tokens / B + 1;
-  if (tbl_entries > kMaxItemBlocks) {
-    msg = "split_tokens / block_size must be below 256";
+  const int tbl_entries = pl.split_tokens / pl.stage_rows + 1;  // copy units of one work item
+  if (tbl_entries > kMaxItemUnits) {
+    msg = "split_tokens / min(block_size, stage tokens) must be below 256";
     return PA_EINVAL;
   }
   auto up = [](size_t x, size_t al) { return (x + al - 1) / al * al; };
@@ -255,9 +258,9 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
   if (a.num_seqs == 0) return PA_OK;
 
   CUtensorMap kmap, vmap;
-  st = encode_pool_map(&kmap, a.k_pool, a, pl.elt, msg);
+  st = encode_pool_map(&kmap, a.k_pool, a, pl.elt, pl.stage_rows, msg);
   if (st != PA_OK) return st;
-  st = encode_pool_map(&vmap, a.v_pool, a, pl.elt, msg);
+  st = encode_pool_map(&vmap, a.v_pool, a, pl.elt, pl.stage_rows, msg);
   if (st != PA_OK) return st;
 
   DecodeParams p{};
@@ -271,6 +274,7 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
   p.log2_block = log2i(a.block_size);
+  p.log2_srows = log2i(pl.stage_rows);
   p.num_blocks = a.num_blocks;
   p.max_blocks = a.max_blocks_per_seq;
   p.max_ctx = a.max_ctx_len;

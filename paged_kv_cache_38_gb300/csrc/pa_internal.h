@@ -18,8 +18,9 @@ struct DecodeParams;
 struct DecodePlan {
   int elt = 2;             // bytes per KV element
   int regions = 1;         // 128-byte column regions per token row
-  int stage_tokens = 16;   // tokens per pipeline stage (16, or 32 for 1-byte KV; >= block_size)
-  int region_stride = 0;   // bytes of one region of one block inside a stage
+  int stage_tokens = 16;   // tokens per pipeline stage (16, or 32 for 1-byte KV; <= 4 blocks)
+  int stage_rows = 16;     // rows of one copy: min(block_size, stage_tokens)
+  int region_stride = 0;   // bytes of one region of one copy inside a stage
   int stage_bytes = 0;     // bytes of K (or V) per stage
   int stages = 0;          // ring depth
   int split_tokens = 0;    // tokens per work item

@@ -22,6 +22,12 @@ def _specs():
         synth.DecodeSpec("e4m3_g16_b32", 3, 32, 2, 128, 32, "e4m3", "f16", ctx_range=(40, 260)),
         S["gqa_pressure"].scaled(name="gqa_small", num_seqs=12, ctx_range=(40, 700),
                                  shared_prompt=64),
+        # blocks larger than a pipeline stage: each copy brings part of one block
+        synth.DecodeSpec("bf16_g4_b64", 5, 16, 4, 128, 64, "bf16", "bf16", ctx_range=(1, 700)),
+        synth.DecodeSpec("f16_g8_d64_b64", 4, 16, 2, 64, 64, "f16", "f16", ctx_range=(1, 400)),
+        synth.DecodeSpec("e4m3_g4_b64", 4, 16, 4, 128, 64, "e4m3", "bf16", ctx_range=(1, 600)),
+        synth.DecodeSpec("bf16_g2_b32", 4, 8, 4, 128, 32, "bf16", "bf16", ctx_range=(1, 300)),
+        synth.DecodeSpec("f16_g1_b64", 3, 4, 4, 128, 64, "f16", "f16", ctx_range=(1, 300)),
     ]
     return pins.small_specs() + extra
 
@@ -51,7 +57,7 @@ def test_decode_matches_oracle(spec, split):
 
 def test_decode_edge_lengths():
     """Empty, single-token, block-boundary and full-capacity contexts, NaN in stale slots."""
-    for B in (4, 8, 16, 32):
+    for B in (4, 8, 16, 32, 64):
         lens = [0, 1, B - 1, B, B + 1, 2 * B - 1, 2 * B, 2 * B + 1, 10 * B, 10 * B - 3]
         spec = synth.DecodeSpec(f"edge_b{B}", len(lens), 8, 2, 128, B, "bf16", "bf16",
                                 ctx_lens=tuple(lens))
