@@ -242,6 +242,103 @@ int pao_decode(const void* q, int q_dtype, const void* k_pool, const void* v_poo
   return bad ? -1 : 0;
 }
 
+/* ---------------------------------------------------------------- prefill attention */
+
+/*
+ * Causal attention of a chunk of new tokens over the paged cache ([PA] prompt phase: all prompt
+ * tokens processed at once, building their KV; [P1] Figure 3: a recomputed request processes
+ * all its retained tokens together; [CB] chunked prefill). Sequence s holds L = ctx_lens[s]
+ * positions (its chunk's K/V already written); its chunk has n = q_starts[s + 1] - q_starts[s]
+ * query tokens, q rows q_starts[s] .. q_starts[s + 1] - 1, and query i stands at position
+ * L - n + i. For each query head h (kv group g = h / (Hq / Hkv)):
+ *   s_t = scale * sum_d q[h][d] * K^[t][d]  for t <= L - n + i;  out = sum_t softmax(s)_t V^[t],
+ * with K^, V^ gathered through the block table as in pao_decode. Returns 0, or -1 if some
+ * length or block id is invalid (those rows are zero).
+ */
+int pao_prefill(const void* q, const void* k_pool, const void* v_pool, int dtype,
+                const int32_t* block_tables, const int32_t* ctx_lens, const int32_t* q_starts,
+                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                int num_blocks, int max_blocks_per_seq, double scale, double* out,
+                int num_threads) {
+  if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
+  const int group = num_q_heads / num_kv_heads;
+  int bad = 0;
+  const int threads = num_threads > 0 ? num_threads : pao_max_threads();
+  (void)threads;
+#pragma omp parallel for collapse(2) schedule(dynamic) num_threads(threads) reduction(| : bad)
+  for (int s = 0; s < num_seqs; ++s) {
+    for (int h = 0; h < num_q_heads; ++h) {
+      const int L = ctx_lens[s];
+      const int n = q_starts[s + 1] - q_starts[s];
+      for (int i = 0; i < n; ++i) {
+        double* o = out + ((size_t)(q_starts[s] + i) * num_q_heads + h) * head_dim;
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+      }
+      if (n <= 0) continue;
+      if (n > L || L > max_blocks_per_seq * block_size) {
+        bad = 1;
+        continue;
+      }
+      const int g = h / group;
+
+      /* 1. gather the sequence's keys and values into contiguous rows */
+      double* K = (double*)malloc(sizeof(double) * (size_t)L * head_dim);
+      double* V = (double*)malloc(sizeof(double) * (size_t)L * head_dim);
+      double* score = (double*)malloc(sizeof(double) * (size_t)L);
+      int rows_ok = 1;
+      for (int t = 0; t < L && rows_ok; ++t) {
+        const int phys = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+        if (phys < 0 || phys >= num_blocks) {
+          rows_ok = 0;
+          break;
+        }
+        const size_t first =
+            (((size_t)phys * num_kv_heads + g) * block_size + t % block_size) * head_dim;
+        for (int d = 0; d < head_dim; ++d) {
+          K[(size_t)t * head_dim + d] = element(k_pool, first + d, dtype);
+          V[(size_t)t * head_dim + d] = element(v_pool, first + d, dtype);
+        }
+      }
+      if (!rows_ok) {
+        bad = 1;
+        free(K);
+        free(V);
+        free(score);
+        continue;
+      }
+
+      /* 2. each query: ordinary softmax attention over positions 0 .. its own */
+      for (int i = 0; i < n; ++i) {
+        const int last = L - n + i;
+        const size_t qoff = ((size_t)(q_starts[s] + i) * num_q_heads + h) * head_dim;
+        double max_score = -INFINITY;
+        for (int t = 0; t <= last; ++t) {
+          double dot = 0.0;
+          for (int d = 0; d < head_dim; ++d)
+            dot += element(q, qoff + d, dtype) * K[(size_t)t * head_dim + d];
+          score[t] = scale * dot;
+          if (score[t] > max_score) max_score = score[t];
+        }
+        double denom = 0.0;
+        for (int t = 0; t <= last; ++t) {
+          score[t] = exp(score[t] - max_score);
+          denom += score[t];
+        }
+        double* o = out + ((size_t)(q_starts[s] + i) * num_q_heads + h) * head_dim;
+        for (int d = 0; d < head_dim; ++d) {
+          double acc = 0.0;
+          for (int t = 0; t <= last; ++t) acc += score[t] * V[(size_t)t * head_dim + d];
+          o[d] = acc / denom;
+        }
+      }
+      free(K);
+      free(V);
+      free(score);
+    }
+  }
+  return bad ? -1 : 0;
+}
+
 /* ---------------------------------------------------------------- block movers */
 
 /*

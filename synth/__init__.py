@@ -357,6 +357,29 @@ def _poison_unused(pool: torch.Tensor, asg: Assignment, spec: DecodeSpec) -> Non
             raw[phys, :, L % B:, :] = bits
 
 
+def prefill_queries(case: PagedCase, seed: int, *, max_chunk: Optional[int] = None,
+                    whole: bool = False) -> Tuple[torch.Tensor, torch.Tensor]:
+    """A chunk of new query tokens per sequence for a prefill over ``case``'s cache: each
+    sequence gets n in [1, L] tokens (all L when ``whole``; at most ``max_chunk``), standing at
+    its last n positions. Returns (q_starts int32 [N + 1], q [total][Hq][D] in the q dtype), on
+    the case's device."""
+    spec = case.spec
+    rng = np.random.default_rng(seed)
+    lens = case.ctx_lens.cpu().numpy()
+    n = np.zeros(len(lens), dtype=np.int64)
+    for s, L in enumerate(lens):
+        if L <= 0:
+            continue
+        hi = int(L) if max_chunk is None else min(int(L), max_chunk)
+        n[s] = hi if whole else int(rng.integers(1, hi + 1))
+    starts = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    dev = case.q.device
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    q = torch.randn((int(starts[-1]), spec.num_q_heads, spec.head_dim), generator=gen, device=dev)
+    return torch.from_numpy(starts).to(dev), q.to(TORCH_DTYPES[spec.q_dtype])
+
+
 def swap_plan(case: PagedCase, seq: int, seed: int) -> Tuple[np.ndarray, np.ndarray]:
     """Blocks of ``seq`` to swap out and a seeded choice of free blocks to swap them into
     ("When KV Capacity Runs Out", Figure 4: restored blocks may sit elsewhere)."""

@@ -353,6 +353,81 @@ def pin_write_kv_fp8(orc):
         assert rc == -1 and np.array_equal(kp, kp2)
 
 
+def _prefill_specs():
+    S = synth.SPECS
+    return [
+        S["mha7b"].scaled(num_seqs=3, ctx_range=(17, 61), num_blocks=None),
+        S["gqa_pressure"].scaled(num_seqs=5, ctx_range=(20, 90), shared_prompt=32),
+        synth.DecodeSpec("g2_b8", 3, 8, 4, 64, 8, "bf16", "bf16", ctx_range=(1, 40)),
+        synth.DecodeSpec("g16_b32", 2, 16, 1, 128, 32, "f16", "f16", ctx_range=(30, 70)),
+    ]
+
+
+def _run_prefill(orc, case, qs, q):
+    spec = case.spec
+    return orc.prefill(q, case.k_pool, case.v_pool, case.block_tables, case.ctx_lens, qs,
+                       dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
+                       num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                       block_size=spec.block_size, scale=case.scale)
+
+
+def pin_prefill_equals_library_attention(orc):
+    """A chunk of n new tokens over a cache of L positions: query i, at position L - n + i,
+    attends to positions 0 .. L - n + i. torch SDPA in fp64 on the unpaged data with that
+    boolean mask (enable_gqa groups query heads contiguously) must agree, for whole prompts
+    (n = L, the prompt phase) and partial chunks (recompute, chunked prefill)."""
+    for i, spec in enumerate(_prefill_specs()):
+        case = synth.make_case(spec, seed=500 + i)
+        for whole in (False, True):
+            qs, q = synth.prefill_queries(case, seed=40 + i, whole=whole)
+            got = _run_prefill(orc, case, qs, q)
+            for s in range(spec.num_seqs):
+                L, a, b = int(case.ctx_lens[s]), int(qs[s]), int(qs[s + 1])
+                n = b - a
+                if n == 0:
+                    continue
+                K, V = logical_values(case, s)
+                qq = q[a:b].to(torch.float64).permute(1, 0, 2)[None]
+                mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+                ref = F.scaled_dot_product_attention(qq, K[None], V[None], attn_mask=mask,
+                                                     scale=case.scale, enable_gqa=True)
+                err = np.abs(got[a:b] - ref[0].permute(1, 0, 2).numpy()).max()
+                assert err < 1e-12, (spec.name, whole, s, err)
+
+
+def pin_prefill_one_token_is_decode(orc):
+    """A chunk of one token is a decode step: the pinned decode oracle, fed that token as its
+    query, gives the same output."""
+    for i, spec in enumerate(_prefill_specs()):
+        case = synth.make_case(spec, seed=520 + i)
+        qs, q = synth.prefill_queries(case, seed=60 + i, max_chunk=1)
+        got = _run_prefill(orc, case, qs, q)
+        ok = (qs[1:] - qs[:-1]) == 1
+        dq = case.q.clone()
+        dq[ok] = q
+        ref = run_decode(orc, case, q=dq)
+        assert np.abs(got - ref[ok.numpy()]).max() < 1e-12, spec.name
+
+
+def pin_prefill_closed_forms(orc):
+    """One cached position attended by itself gives its value row; a query of zeros weighs all
+    visible positions equally (mean of the values it may see)."""
+    spec = synth.DecodeSpec("pf_one", 3, 4, 2, 64, 4, "f16", "f16", ctx_lens=(1, 9, 13))
+    case = synth.make_case(spec, seed=3)
+    qs = torch.tensor([0, 1, 4, 9], dtype=torch.int32)
+    q = torch.randn(9, 4, 64, generator=torch.Generator().manual_seed(1)).to(torch.float16)
+    q[1:4] = 0
+    got = _run_prefill(orc, case, qs, q)
+    K, V = logical_values(case, 0)
+    for h in range(4):
+        assert np.array_equal(got[0, h], V[h // 2, 0].numpy())
+    K, V = logical_values(case, 1)
+    for i in range(3):  # positions 6, 7, 8 of a 9-position cache
+        for h in range(4):
+            want = V[h // 2, : 6 + i + 1].mean(0).numpy()
+            assert np.abs(got[1 + i, h] - want).max() < 1e-12
+
+
 def _toy_script():
     with open(os.path.join(GOLDEN, "toy_figures_1_2.txt")) as f:
         return [ln.split() for ln in (l.split("#")[0].strip() for l in f) if ln]
@@ -511,4 +586,6 @@ ALL_PINS = [
     pin_closed_forms, pin_scales, pin_group_equals_replicated_heads, pin_permutation_invariance,
     pin_bounds, pin_write_kv, pin_toy_figures, pin_toy_permuted, pin_copy_on_write,
     pin_swap_round_trip, pin_e4m3_encoder, pin_write_kv_fp8,
+    pin_prefill_equals_library_attention, pin_prefill_one_token_is_decode,
+    pin_prefill_closed_forms,
 ]
