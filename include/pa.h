@@ -138,6 +138,51 @@ size_t pa_decode_workspace_size(const pa_decode_args* args);
 pa_status pa_decode(const pa_decode_args* args, pa_stream stream);
 
 /*
+ * pa_prefill - causal attention of chunks of new tokens over the paged KV pool (prompt
+ * processing, recomputation of a preempted request, chunked prefill).
+ *
+ * Source: PagedAttention summary page, paragraph on the two phases (the prompt phase processes
+ * all prompt tokens at once, matrix-matrix work that builds their KV cache); "When KV Capacity
+ * Runs Out", Figure 3 (a recomputed request feeds all its retained tokens together); the block
+ * table as in pa_decode. Sequence s holds L = ctx_lens[s] positions, including its chunk's own
+ * K/V (written first with pa_write_kv); its chunk is the n = q_starts[s + 1] - q_starts[s] query
+ * rows q_starts[s] .. q_starts[s + 1] - 1, query i standing at position L - n + i. For query
+ * head h (group g = h / (num_q_heads / num_kv_heads)):
+ *     out[q_starts[s] + i][h] = sum_{t <= L - n + i} softmax_t(scale * <q, K^[t]>) V^[t]
+ * computed on the tensor cores (tcgen05.mma, fp32 accumulation in tensor memory).
+ *   q, out        device [num_tokens][num_q_heads][head_dim], dtype, 16-byte aligned
+ *   q_starts      device int32 [num_seqs + 1], non-decreasing, q_starts[num_seqs] = num_tokens
+ *   max_q_len     host upper bound of the chunk lengths (sizes the grid)
+ * A sequence with n > L or L > max_blocks_per_seq * block_size sets PA_ERR_CTX_LEN and its rows
+ * are zero; an out-of-pool block id sets PA_ERR_BLOCK_ID (those rows are then unspecified).
+ * Supported: dtype PA_F16 or PA_BF16 (q, K/V and out alike); head_dim 64 or 128; block_size 8,
+ * 16, 32 or 64; group size 1, 2, 4, 8 or 16.
+ */
+typedef struct {
+  const void* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* block_tables;
+  const int32_t* ctx_lens;
+  const int32_t* q_starts;
+  void* out;
+  int32_t num_seqs;
+  int32_t num_tokens;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t max_q_len;
+  pa_dtype dtype;
+  float scale;
+  int32_t* err_flag;     /* device int32 or NULL */
+} pa_prefill_args;
+
+pa_status pa_prefill(const pa_prefill_args* args, pa_stream stream);
+
+/*
  * pa_write_kv - store each new token's key and value in its slot.
  *
  * Source: "When KV Capacity Runs Out", section "Pause requests and release KV blocks"

@@ -62,6 +62,12 @@ pa_status pa_decode(const pa_decode_args* args, pa_stream stream) {
   return finish(pa::run_decode(*args, reinterpret_cast<cudaStream_t>(stream), msg), msg);
 }
 
+pa_status pa_prefill(const pa_prefill_args* args, pa_stream stream) {
+  std::string msg;
+  if (args == nullptr) return finish(PA_EINVAL, "args is NULL");
+  return finish(pa::run_prefill(*args, reinterpret_cast<cudaStream_t>(stream), msg), msg);
+}
+
 pa_status pa_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
                       const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
                       int32_t head_dim, int32_t block_size, int32_t num_blocks, pa_dtype kv_dtype,

@@ -37,14 +37,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // one copy: `rows` token rows of one (block, kv head) tile x 128 bytes, 128-byte swizzle.
 pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_decode_args& a, int elt,
                           int box_rows, std::string& msg) {
+  return encode_pool_rows_map(map, pool, static_cast<long long>(a.num_blocks) * a.num_kv_heads *
+                                             a.block_size,
+                              a.head_dim, elt, box_rows, msg);
+}
+
+}  // namespace
+
+// The pool as a 2-D tensor [rows][head_dim] of elt-byte elements with a box of box_rows rows x
+// 128 bytes, 128-byte swizzle (the shared-memory operand layout of the decode and prefill
+// kernels).
+pa_status encode_pool_rows_map(CUtensorMap* map, const void* pool, long long rows, int head_dim,
+                               int elt, int box_rows, std::string& msg) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) {
     msg = "cuTensorMapEncodeTiled is not available from the driver";
     return PA_ECUDA;
   }
-  const cuuint64_t rows = static_cast<cuuint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.head_dim), rows};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.head_dim) * elt};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elt};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, elt == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
@@ -57,8 +68,6 @@ pa_status encode_pool_map(CUtensorMap* map, const void* pool, const pa_decode_ar
   }
   return PA_OK;
 }
-
-}  // namespace
 
 pa_status cuda_status(cudaError_t e, const char* what, std::string& msg) {
   if (e == cudaSuccess) return PA_OK;

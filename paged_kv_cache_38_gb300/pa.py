@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.pa_decode.argtypes = [ctypes.POINTER(pa_decode_args), _vp]
         L.pa_write_kv.restype = ctypes.c_int
         L.pa_write_kv.argtypes = [_vp] * 5 + [_i32] * 5 + [ctypes.c_int, _vp, _vp]
+        L.pa_prefill.restype = ctypes.c_int
+        L.pa_prefill.argtypes = [ctypes.POINTER(pa_prefill_args), _vp]
         L.pa_write_kv_fp8.restype = ctypes.c_int
         L.pa_write_kv_fp8.argtypes = [_vp, _vp, ctypes.c_int, _vp, _vp, _vp] + [_i32] * 5 + [
             ctypes.c_float, ctypes.c_float, _vp, _vp]
@@ -184,6 +186,47 @@ def pa_decode_static_workspace(q: torch.Tensor, k_pool: torch.Tensor, v_pool: to
                             k_scale=k_scale, v_scale=v_scale, max_ctx_len=max_ctx_len,
                             split_tokens=split_tokens, err_flag=err_flag)
     _check(lib().pa_decode_static_workspace(ctypes.byref(args), _stream(stream)))
+    return out
+
+
+class pa_prefill_args(ctypes.Structure):
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p), ("ctx_lens", ctypes.c_void_p),
+        ("q_starts", ctypes.c_void_p), ("out", ctypes.c_void_p), ("num_seqs", ctypes.c_int32),
+        ("num_tokens", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
+        ("dtype", ctypes.c_int), ("scale", ctypes.c_float), ("err_flag", ctypes.c_void_p),
+    ]
+
+
+def pa_prefill(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+               block_tables: torch.Tensor, ctx_lens: torch.Tensor, q_starts: torch.Tensor,
+               scale: float, *, out: Optional[torch.Tensor] = None,
+               max_q_len: Optional[int] = None, err_flag: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's chunk of query tokens (rows q_starts[s] ..
+    q_starts[s + 1] - 1 of q [num_tokens][num_q_heads][head_dim]) over its paged cache."""
+    if out is None:
+        out = torch.empty_like(q)
+    dt = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}.get(q.dtype)
+    if dt is None:
+        raise PaError(PA_EINVAL, "q must be float16 or bfloat16")
+    if max_q_len is None:
+        max_q_len = int((q_starts[1:] - q_starts[:-1]).max().item()) if q_starts.numel() > 1 else 0
+    a = pa_prefill_args()
+    a.q, a.k_pool, a.v_pool = q.data_ptr(), k_pool.data_ptr(), v_pool.data_ptr()
+    a.block_tables, a.ctx_lens = block_tables.data_ptr(), ctx_lens.data_ptr()
+    a.q_starts, a.out = q_starts.data_ptr(), out.data_ptr()
+    a.num_seqs = ctx_lens.numel()
+    a.num_tokens, a.num_q_heads, a.head_dim = q.shape[0], q.shape[1], q.shape[2]
+    a.num_kv_heads, a.block_size, a.num_blocks = k_pool.shape[1], k_pool.shape[2], k_pool.shape[0]
+    a.max_blocks_per_seq = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    a.max_q_len, a.dtype, a.scale = int(max_q_len), dt, float(scale)
+    a.err_flag = _ptr(err_flag)
+    _check(lib().pa_prefill(ctypes.byref(a), _stream(stream)))
     return out
 
 

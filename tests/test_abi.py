@@ -27,7 +27,7 @@ def declared_functions(header=None):
 def test_header_declares_the_boundary():
     assert declared_functions(HEADER) == sorted([
         "pa_copy_blocks", "pa_decode", "pa_decode_static_workspace", "pa_decode_workspace_size",
-        "pa_last_error_message", "pa_status_string", "pa_swap_blocks", "pa_write_kv",
+        "pa_last_error_message", "pa_prefill", "pa_status_string", "pa_swap_blocks", "pa_write_kv",
         "pa_write_kv_fp8"])
     assert declared_functions(os.path.join(os.path.dirname(HEADER), "pa_scheduler.h")) == sorted([
         "pa_scheduler_add_request", "pa_scheduler_create", "pa_scheduler_destroy",
@@ -46,6 +46,7 @@ def test_library_exports_every_declared_symbol():
 
 @pytest.mark.parametrize("name,header,cls", [
     ("pa_decode_args", "pa.h", lambda: pa.pa.pa_decode_args),
+    ("pa_prefill_args", "pa.h", lambda: pa.pa.pa_prefill_args),
     ("pa_step_plan", "pa_scheduler.h", lambda: __import__(
         "paged_kv_cache_38_gb300.scheduler", fromlist=["x"]).pa_step_plan)])
 def test_struct_layout_matches_header(tmp_path, name, header, cls):

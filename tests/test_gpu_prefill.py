@@ -1,0 +1,94 @@
+"""pa_prefill (tcgen05 tensor cores) against the fp64 oracle, through the C ABI (needs a GB300).
+
+Each sequence's chunk of n new tokens stands at its last n cache positions and attends
+causally; whole prompts (n = L), partial chunks and one-token chunks; stale slots and free
+blocks hold NaN, so any read past a sequence's context shows."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import TOL
+
+import paged_kv_cache_38_gb300 as pa  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+SPECS = [
+    synth.DecodeSpec("pf_bf16_g4_b16", 6, 16, 4, 128, 16, "bf16", "bf16", ctx_range=(1, 300)),
+    synth.DecodeSpec("pf_f16_g1_b16", 4, 4, 4, 128, 16, "f16", "f16", ctx_range=(1, 260)),
+    synth.DecodeSpec("pf_bf16_g8_d64_b32", 5, 16, 2, 64, 32, "bf16", "bf16", ctx_range=(1, 200)),
+    synth.DecodeSpec("pf_f16_g16_b64", 3, 32, 2, 128, 64, "f16", "f16", ctx_range=(1, 330)),
+    synth.DecodeSpec("pf_bf16_g2_d64_b8", 5, 8, 4, 64, 8, "bf16", "bf16", ctx_range=(1, 150)),
+]
+CHUNKS = ["whole", "partial", "one"]
+
+
+def _oracle(case, qs, q):
+    spec = case.spec
+    return oracle.load().prefill(q.cpu(), case.k_pool.cpu(), case.v_pool.cpu(),
+                                 case.block_tables.cpu(), case.ctx_lens.cpu(), qs.cpu(),
+                                 dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
+                                 num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                                 block_size=spec.block_size, scale=case.scale)
+
+
+def _err(out, ref):
+    g = out.double().cpu().numpy()
+    return float(np.abs(g - ref).max()) if np.all(np.isfinite(g)) else float("inf")
+
+
+@pytest.mark.parametrize("spec,chunk", [(s, c) for s in SPECS for c in CHUNKS],
+                         ids=[f"{s.name}-{c}" for s in SPECS for c in CHUNKS])
+def test_prefill_matches_oracle(spec, chunk):
+    case = synth.make_case(spec, seed=700)
+    qs, q = synth.prefill_queries(case, seed=7, whole=chunk == "whole",
+                                  max_chunk=1 if chunk == "one" else None)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qs.cuda(),
+                        case.scale, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    e = _err(out, ref)
+    assert e <= TOL[spec.kv_dtype], f"{spec.name} {chunk}: max abs err {e}"
+
+
+def test_prefill_long_chunks():
+    """Long prompts and chunks (several query tiles and many key tiles per sequence)."""
+    spec = synth.DecodeSpec("pf_long", 3, 32, 8, 128, 16, "bf16", "bf16", ctx_lens=(1500, 777, 2048))
+    case = synth.make_case(spec, seed=71)
+    qs = torch.tensor([0, 1500, 1500 + 300, 1500 + 300 + 1024], dtype=torch.int32)
+    q = torch.randn(int(qs[-1]), 32, 128, generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qs.cuda(),
+                        case.scale)
+    torch.cuda.synchronize()
+    assert _err(out, ref) <= TOL["bf16"]
+
+
+def test_prefill_bad_lengths_flagged():
+    spec = synth.DecodeSpec("pf_bad", 3, 8, 2, 128, 16, "bf16", "bf16", ctx_lens=(40, 40, 40))
+    case = synth.make_case(spec, seed=5).to("cuda")
+    qs = torch.tensor([0, 10, 60, 70], dtype=torch.int32, device="cuda")  # 50 > 40 for seq 1
+    q = torch.randn(70, 8, 128, device="cuda").to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pa.pa_prefill(q, case.k_pool, case.v_pool, case.block_tables, case.ctx_lens, qs,
+                        case.scale, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_ERR_CTX_LEN
+    assert torch.count_nonzero(out[10:60]).item() == 0
+    ref = _oracle(case, qs.cpu(), q.cpu())
+    assert _err(out[:10], ref[:10]) <= TOL["bf16"] and _err(out[60:], ref[60:]) <= TOL["bf16"]
+
+
+def test_prefill_host_validation():
+    case = synth.make_case(synth.SPECS["toy"], seed=1).to("cuda")  # block_size 4: not built
+    qs = torch.tensor([0, 1, 2], dtype=torch.int32, device="cuda")
+    q = torch.randn(2, 4, 64, device="cuda").to(torch.float16)
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_prefill(q, case.k_pool, case.v_pool, case.block_tables, case.ctx_lens, qs, 0.125)
+    assert e.value.status == pa.PA_EUNSUPPORTED
