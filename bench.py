@@ -104,8 +104,9 @@ def load_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
 def decode_source_hash() -> str:
@@ -452,7 +453,51 @@ def run_extras(args, dev, flush, peaks) -> dict:
     res["write_kv_fp8"] = run_quantise_bench(dev, flush, peaks)
     res["scheduler"] = run_scheduler_bench(dev)
     res["block_size_sweep"] = run_block_sweep(dev, flush, peaks)
+    res["prefill"] = run_prefill_bench(dev, flush, peaks)
     return res
+
+
+def prefill_flops(ctx_lens, q_starts, num_q_heads: int, head_dim: int) -> int:
+    """Causal attention work of a prefill: query i of a chunk of n over L positions sees
+    L - n + i + 1 keys; each key costs 2 D flops for Q K^T and 2 D for P V, per query head."""
+    total = 0
+    for s in range(len(ctx_lens)):
+        L, n = int(ctx_lens[s]), int(q_starts[s + 1] - q_starts[s])
+        first = L - n + 1
+        total += n * first + n * (n - 1) // 2
+    return 4 * head_dim * num_q_heads * total
+
+
+def run_prefill_bench(dev, flush, peaks) -> dict:
+    """pa_prefill on the GQA geometry (32 q / 8 kv heads x 128, bf16, 16-token blocks):
+    16 whole 2,048-token prompts, and 64 chunks of 512 new tokens on 1,536-token histories
+    (chunked prefill / recompute). Causal flops per second against the measured bf16 GEMM
+    peak."""
+    import paged_kv_cache_38_gb300 as pa
+
+    out = {}
+    for name, lens, chunk in (("prompts_16x2048", [2048] * 16, 2048),
+                              ("chunks_64x512_on_2048", [2048] * 64, 512)):
+        spec = synth.DecodeSpec(name, len(lens), 32, 8, 128, 16, "bf16", "bf16",
+                                ctx_lens=tuple(lens))
+        case = synth.make_case(spec, seed=SEED, device=dev, logical=False, poison=False)
+        n = [chunk] * len(lens)
+        qs = torch.tensor(np.concatenate([[0], np.cumsum(n)]), dtype=torch.int32, device=dev)
+        q = torch.randn(int(qs[-1]), 32, 128, device=dev).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        call = lambda: pa.pa_prefill(q, case.k_pool, case.v_pool, case.block_tables,  # noqa: E731
+                                     case.ctx_lens, qs, case.scale, out=o, max_q_len=chunk)
+        for _ in range(3):
+            call()
+        t = statistics.mean(time_steps(call, 10, flush))
+        fl = prefill_flops(lens, qs.cpu().numpy(), 32, 128)
+        tf = fl / (t * 1e-3) / 1e12
+        out[name] = {"ms": round(t, 4), "tflops": round(tf, 1),
+                     "pct_of_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 1),
+                     "tokens_per_s": round(int(qs[-1]) / (t * 1e-3), 1)}
+        del case, q, o
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_block_sweep(dev, flush, peaks) -> dict:

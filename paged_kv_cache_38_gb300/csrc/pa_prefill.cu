@@ -8,7 +8,8 @@
 //
 // GB300 design: one CTA per (sequence, kv head, tile of 128 query rows); a row is one (token,
 // query head of the group), so a tile holds 128 / G tokens and the GQA group shares every K/V
-// tile. K/V tiles of 64 keys stream through a 3-stage shared-memory ring:
+// tile. K/V tiles of 64 keys stream through a 2-stage shared-memory ring (about 113 KB per CTA
+// at head_dim 128, so two CTAs share an SM and overlap each other's softmax and MMA phases):
 //   * warp 0 issues 2-D TMA copies of each tile through the block table (copy units of
 //     min(block_size, 64) rows, 128-byte swizzle);
 //   * warp 1 allocates tensor memory and one lane issues the MMAs: S_j = Q K_j^T (M 128, N 64)
@@ -39,7 +40,7 @@ namespace {
 constexpr int kPfThreads = 256;   // 8 warps
 constexpr int kPfRows = 128;      // query rows per tile = MMA M
 constexpr int kPfKeys = 64;       // keys per K/V tile: S columns, PV reduction
-constexpr int kPfStages = 3;      // K/V ring depth
+constexpr int kPfStages = 2;      // K/V ring depth (two CTAs fit on an SM)
 constexpr int kSoftmaxWarp0 = 4;  // warps 4..7 form the softmax warpgroup
 constexpr uint32_t kTmemCols = 256;  // O at columns [0, head_dim), S buffers at [128, 192), [192, 256)
 
@@ -106,10 +107,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     return;
   }
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* bp = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_addr(smem_raw);
+  uint8_t* bp = smem_raw;
+  if ((base & 1023u) != 0) {  // the swizzled operands need 1024-byte alignment
+    if (tid == 0) flag_error(p.err, kErrTimeout);
+    return;
+  }
   const uint32_t sQ = base;
   const uint32_t sKV = sQ + kRegions * kQRegion;  // stage st: K at sKV + 2 st kKVBytes, V after it
   const uint32_t sP = sKV + kPfStages * 2 * kKVBytes;
@@ -170,6 +174,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int units = kPfKeys >> p.log2_urows;
       prefetch_tensormap(&kmap);
       prefetch_tensormap(&vmap);
+      // The block-table entries of tile j + 1 are read while the producer waits for a free
+      // stage for tile j + 1, so their latency is off the copy path.
+      int ph[8];
+      auto load_phys = [&](int j) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int key = j * kPfKeys + u * urows;
+          ph[u] = (u < units && key < L) ? __ldg(trow + (key >> p.log2_block)) : -2;
+        }
+      };
+      load_phys(0);
       int issued = 0;
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % kPfStages;
@@ -184,16 +199,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         uint32_t bytes = 0;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          rowc[u] = -1;
           const int key = j * kPfKeys + u * urows;
-          if (u < units && key < L) {
-            const int ph = __ldg(trow + (key >> p.log2_block));
-            if (ph < 0 || ph >= p.num_blocks) {
-              flag_error(p.err, kErrBlockId);
-            } else {
-              rowc[u] = (ph * p.num_kv_heads + g) * B + (key & (B - 1));
-              bytes += 2u * kRegions * static_cast<uint32_t>(urows) * 128u;
-            }
+          rowc[u] = -1;
+          if (ph[u] == -2) continue;  // past the unit count or the cache
+          if (ph[u] < 0 || ph[u] >= p.num_blocks) {
+            flag_error(p.err, kErrBlockId);
+          } else {
+            rowc[u] = (ph[u] * p.num_kv_heads + g) * B + (key & (B - 1));
+            bytes += 2u * kRegions * static_cast<uint32_t>(urows) * 128u;
           }
         }
         const uint32_t full = smem_addr(kv_full + st);
@@ -210,6 +223,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
         issued = j + 1;
+        if (j + 1 < ntiles) load_phys(j + 1);
       }
       // no copy of this CTA may still be landing when it exits (matters after an abort)
       for (int jj = max(0, issued - kPfStages); jj < issued; ++jj)
@@ -277,12 +291,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tc_fence_after();
       float x[kPfKeys];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32_nowait(tS + 64 * b + lane_base, r0);
+        tmem_ld32_nowait(tS + 64 * b + lane_base + 32, r1);
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < kPfKeys; c += 16) {
-        float v[16];
-        tmem_ld16(tS + 64 * b + lane_base + c, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[c + i] = v[i];
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(r0[i]);
+          x[32 + i] = __uint_as_float(r1[i]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -295,8 +313,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         x[c] = (row_valid && key0 + c <= pos) ? x[c] * p.scale_log2 : -INFINITY;
         mt = fmaxf(mt, x[c]);
       }
-      const float m_new = fmaxf(m, mt);
-      const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
+      // Lazy rescaling: the row keeps its reference maximum m unless the tile's maximum exceeds
+      // it by more than 8 (log2 units); weights then stay below 2^8 and O is rescaled rarely.
+      // Numerator and denominator share the same reference, so the result is unchanged.
+      const float m_new = mt > m + 8.f ? mt : m;
+      const float alpha = m_new == m ? 1.f : ex2(m - m_new);
       uint32_t pk[kPfKeys / 2];
       float psum = 0.f;
 #pragma unroll
@@ -363,15 +384,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
                                             (static_cast<size_t>(q0 + tr) * Hq + g * G + r % G) * D);
 #pragma unroll 1
-      for (int c = 0; c < D; c += 16) {
-        float v[16];
-        tmem_ld16(tO + lane_base + c, v);
+      for (int c = 0; c < D; c += 32) {
+        uint32_t v[32];
+        tmem_ld32_nowait(tO + lane_base + c, v);
+        tmem_wait_ld();
         if (row_valid) {
-          uint32_t w[8];
+          uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w[i] = pack16<BF16>(v[2 * i] * inv, v[2 * i + 1] * inv);
-          dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack16<BF16>(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[c / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
     }
@@ -500,7 +524,9 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
 
   const int D = a.head_dim;
   const size_t regions = static_cast<size_t>(D / 64);
-  const size_t smem = 1024 + regions * kPfRows * 128 + kPfStages * 2 * regions * kPfKeys * 128 +
+  // no alignment slack: the kernel needs (and checks) a 1024-byte aligned dynamic region, and
+  // two CTAs then fit on an SM
+  const size_t smem = regions * kPfRows * 128 + kPfStages * 2 * regions * kPfKeys * 128 +
                       kPfRows * 128 + 256;
   const int tokens_per_tile = kPfRows / group;
   const unsigned tiles = static_cast<unsigned>((a.max_q_len + tokens_per_tile - 1) / tokens_per_tile);
