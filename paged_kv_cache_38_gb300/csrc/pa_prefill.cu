@@ -10,8 +10,8 @@
 // query head of the group), so a tile holds 128 / G tokens and the GQA group shares every K/V
 // tile. K/V tiles of 64 keys stream through a 2-stage shared-memory ring (about 113 KB per CTA
 // at head_dim 128, so two CTAs share an SM and overlap each other's softmax and MMA phases):
-//   * warp 0 issues 2-D TMA copies of each tile through the block table (copy units of
-//     min(block_size, 64) rows, 128-byte swizzle);
+//   * warps 0 and 2 issue 2-D TMA copies of the K and the V tiles through the block table
+//     (copy units of min(block_size, 64) rows, 128-byte swizzle), each through its own ring;
 //   * warp 1 allocates tensor memory and one lane issues the MMAs: S_j = Q K_j^T (M 128, N 64)
 //     into one of two TMEM S buffers, and O += P_{j-1} V_{j-1} (M 128, N = head_dim) into the
 //     TMEM O accumulator, each completion signalled by tcgen05.commit on an mbarrier;
@@ -78,7 +78,7 @@ __device__ __forceinline__ float2 unpack16(uint32_t u) {
 }
 
 template <int D, int G, bool BF16>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(kPfThreads, 2)
     pa_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillParams p) {
   constexpr int kRegions = D / 64;
@@ -118,9 +118,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t sKV = sQ + kRegions * kQRegion;  // stage st: K at sKV + 2 st kKVBytes, V after it
   const uint32_t sP = sKV + kPfStages * 2 * kKVBytes;
   uint8_t* bars_p = bp + (sP - base) + kPfRows * 128;
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(bars_p);  // [kPfStages]
-  uint64_t* kv_empty = kv_full + kPfStages;                  // [kPfStages]
-  uint64_t* s_full = kv_empty + kPfStages;                   // [2]
+  // K and V stream through separate rings: K of tile j is free once S_j is computed, V once
+  // PV_j is, so K loads run a whole softmax ahead of V loads.
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(bars_p);  // [kPfStages]
+  uint64_t* k_empty = k_full + kPfStages;                   // [kPfStages]
+  uint64_t* v_full = k_empty + kPfStages;                   // [kPfStages]
+  uint64_t* v_empty = v_full + kPfStages;                   // [kPfStages]
+  uint64_t* s_full = v_empty + kPfStages;                   // [2]
   uint64_t* s_free = s_full + 2;                             // [2]
   uint64_t* p_full = s_free + 2;
   uint64_t* o_done = p_full + 1;
@@ -146,8 +150,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(smem_addr(kv_full + i), 1);
-      mbar_init(smem_addr(kv_empty + i), 1);
+      mbar_init(smem_addr(k_full + i), 1);
+      mbar_init(smem_addr(k_empty + i), 1);
+      mbar_init(smem_addr(v_full + i), 1);
+      mbar_init(smem_addr(v_empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(s_full + i), 1);
@@ -165,15 +171,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem, tS = tmem + 128;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ K/V producer
+  if (warp == 0 || warp == 2) {
+    // ------------------------------------------------------------------ K/V producers
+    // warp 0 streams K, warp 2 streams V, each through its own ring (two lanes of one warp
+    // would hold each other up in their barrier waits)
     if (lane == 0) {
+      const bool is_v = warp == 2;
+      const CUtensorMap* map = is_v ? &vmap : &kmap;
+      uint64_t* fullb = is_v ? v_full : k_full;
+      uint64_t* emptyb = is_v ? v_empty : k_empty;
       const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
       const uint64_t pol = policy_evict_normal();  // the sequence's other query tiles reread them
       const int urows = 1 << p.log2_urows, B = p.block_size;
       const int units = kPfKeys >> p.log2_urows;
-      prefetch_tensormap(&kmap);
-      prefetch_tensormap(&vmap);
+      prefetch_tensormap(map);
       // The block-table entries of tile j + 1 are read while the producer waits for a free
       // stage for tile j + 1, so their latency is off the copy path.
       int ph[8];
@@ -189,7 +200,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int j = 0; j < ntiles; ++j) {
         const int st = j % kPfStages;
         if (j >= kPfStages &&
-            !mbar_wait_bounded(smem_addr(kv_empty + st), ((j / kPfStages) - 1) & 1)) {
+            !mbar_wait_bounded(smem_addr(emptyb + st), ((j / kPfStages) - 1) & 1)) {
           flag_error(p.err, kErrTimeout);
           *abort_flag = 1;
           break;
@@ -203,31 +214,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           rowc[u] = -1;
           if (ph[u] == -2) continue;  // past the unit count or the cache
           if (ph[u] < 0 || ph[u] >= p.num_blocks) {
-            flag_error(p.err, kErrBlockId);
+            if (!is_v) flag_error(p.err, kErrBlockId);
           } else {
             rowc[u] = (ph[u] * p.num_kv_heads + g) * B + (key & (B - 1));
-            bytes += 2u * kRegions * static_cast<uint32_t>(urows) * 128u;
+            bytes += static_cast<uint32_t>(kRegions * urows * 128);
           }
         }
-        const uint32_t full = smem_addr(kv_full + st);
+        const uint32_t full = smem_addr(fullb + st);
         mbar_arrive_expect_tx(full, bytes);
-        const uint32_t kdst = sKV + 2 * st * kKVBytes, vdst = kdst + kKVBytes;
+        const uint32_t dst = sKV + 2 * st * kKVBytes + (is_v ? kKVBytes : 0u);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           if (rowc[u] < 0) continue;
 #pragma unroll
-          for (int c = 0; c < kRegions; ++c) {
-            const uint32_t off = c * kKVRegion + static_cast<uint32_t>(u * urows * 128);
-            tma_load_2d(kdst + off, &kmap, c * 64, rowc[u], full, pol);
-            tma_load_2d(vdst + off, &vmap, c * 64, rowc[u], full, pol);
-          }
+          for (int c = 0; c < kRegions; ++c)
+            tma_load_2d(dst + c * kKVRegion + static_cast<uint32_t>(u * urows * 128), map, c * 64,
+                        rowc[u], full, pol);
         }
         issued = j + 1;
         if (j + 1 < ntiles) load_phys(j + 1);
       }
       // no copy of this CTA may still be landing when it exits (matters after an abort)
       for (int jj = max(0, issued - kPfStages); jj < issued; ++jj)
-        mbar_wait_bounded(smem_addr(kv_full + jj % kPfStages), (jj / kPfStages) & 1);
+        mbar_wait_bounded(smem_addr(fullb + jj % kPfStages), (jj / kPfStages) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -238,7 +247,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int j = 0; j <= ntiles && ok; ++j) {
         if (j < ntiles) {
           const int st = j % kPfStages, b = j & 1;
-          ok = mbar_wait_bounded(smem_addr(kv_full + st), (j / kPfStages) & 1) &&
+          ok = mbar_wait_bounded(smem_addr(k_full + st), (j / kPfStages) & 1) &&
                (j < 2 || mbar_wait_bounded(smem_addr(s_free + b), ((j >> 1) - 1) & 1));
           if (!ok || *abort_flag) break;
           tc_fence_after();
@@ -250,10 +259,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                      umma_sdesc(kst + c * kKVRegion + kk * 32, 16, 1024), idS, k > 0);
           }
           umma_commit(smem_addr(s_full + b));
+          umma_commit(smem_addr(k_empty + st));
         }
         if (j >= 1) {
           const int jp = j - 1, stp = jp % kPfStages;
-          ok = mbar_wait_bounded(smem_addr(p_full), jp & 1);
+          ok = mbar_wait_bounded(smem_addr(p_full), jp & 1) &&
+               mbar_wait_bounded(smem_addr(v_full + stp), (jp / kPfStages) & 1);
           if (!ok || *abort_flag) break;
           tc_fence_after();
           const uint32_t vst = sKV + 2 * stp * kKVBytes + kKVBytes;
@@ -262,7 +273,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             umma_f16(tO, umma_sdesc(sP + k * 32, 16, 1024),
                      umma_sdesc(vst + k * 16 * 128, kKVRegion, 1024), idO, jp > 0 || k > 0);
           umma_commit(smem_addr(o_done));
-          umma_commit(smem_addr(kv_empty + stp));
+          umma_commit(smem_addr(v_empty + stp));
         }
       }
       if (!ok) {
@@ -307,12 +318,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (lane == 0) mbar_arrive(smem_addr(s_free + b));
 
       const int key0 = j * kPfKeys;
+      // Rows that see all 64 keys of the tile (every tile before the diagonal) need no mask.
+      // Scores stay raw until the exponent: m is kept in scaled log2 units and the weight of
+      // score x is 2^(x * scale_log2 - m), one FFMA and one ex2.
+      const bool full = row_valid && key0 + kPfKeys - 1 <= pos;
+      const int lim = row_valid ? pos - key0 : -1;  // last visible column (full: >= 63)
       float mt = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < kPfKeys; ++c) {
-        x[c] = (row_valid && key0 + c <= pos) ? x[c] * p.scale_log2 : -INFINITY;
-        mt = fmaxf(mt, x[c]);
+        for (int c = 0; c < kPfKeys; ++c) mt = fmaxf(mt, x[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kPfKeys; ++c)
+          if (c <= lim) mt = fmaxf(mt, x[c]);
       }
+      mt = mt == -INFINITY ? -INFINITY : mt * p.scale_log2;
       // Lazy rescaling: the row keeps its reference maximum m unless the tile's maximum exceeds
       // it by more than 8 (log2 units); weights then stay below 2^8 and O is rescaled rarely.
       // Numerator and denominator share the same reference, so the result is unchanged.
@@ -320,13 +340,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const float alpha = m_new == m ? 1.f : ex2(m - m_new);
       uint32_t pk[kPfKeys / 2];
       float psum = 0.f;
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < kPfKeys; c += 2) {
-        const float p0 = x[c] == -INFINITY ? 0.f : ex2(x[c] - m_new);
-        const float p1 = x[c + 1] == -INFINITY ? 0.f : ex2(x[c + 1] - m_new);
-        pk[c / 2] = pack16<BF16>(p0, p1);
-        const float2 rounded = unpack16<BF16>(pk[c / 2]);  // the weights the MMA will use
-        psum += rounded.x + rounded.y;
+        for (int c = 0; c < kPfKeys; c += 2) {
+          const float p0 = ex2(fmaf(x[c], p.scale_log2, -m_new));
+          const float p1 = ex2(fmaf(x[c + 1], p.scale_log2, -m_new));
+          pk[c / 2] = pack16<BF16>(p0, p1);
+          psum += p0 + p1;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kPfKeys; c += 2) {
+          const float p0 = c <= lim && m_new != -INFINITY ? ex2(fmaf(x[c], p.scale_log2, -m_new)) : 0.f;
+          const float p1 =
+              c + 1 <= lim && m_new != -INFINITY ? ex2(fmaf(x[c + 1], p.scale_log2, -m_new)) : 0.f;
+          pk[c / 2] = pack16<BF16>(p0, p1);
+          psum += p0 + p1;
+        }
       }
       l = l * alpha + psum;
       m = m_new;
@@ -341,7 +371,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       if (j == ntiles - 1 && key0 + kPfKeys > L) {
         // value rows past the cache's last position (stale slots, or not loaded) become zero,
-        // so that zero weights cannot meet a NaN
+        // so that zero weights cannot meet a NaN; the tile's V copies must have landed first
+        ok = mbar_wait_bounded(smem_addr(v_full + (j % kPfStages)), (j / kPfStages) & 1);
+        if (__any_sync(0xffffffffu, !ok)) {
+          ok = false;
+          break;
+        }
         const uint32_t vst = sKV + 2 * ((ntiles - 1) % kPfStages) * kKVBytes + kKVBytes;
         const int r0 = L - key0;
         const int nbytes16 = (kPfKeys - r0) * 8 * kRegions;  // 16-byte chunks to clear
