@@ -243,37 +243,60 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_f16(kPfRows, kPfKeys, BF16, false);
       constexpr uint32_t idO = umma_idesc_f16(kPfRows, D, BF16, true);
+      // Issue S_ns as soon as K_ns has landed (and its S buffer is free), and PV_npv as soon as
+      // P_npv and V_npv are ready, whichever comes first: a late K tile does not hold up the
+      // PV of the previous tile. PVs go in tile order (they accumulate into O).
       bool ok = true;
-      for (int j = 0; j <= ntiles && ok; ++j) {
-        if (j < ntiles) {
-          const int st = j % kPfStages, b = j & 1;
-          ok = mbar_wait_bounded(smem_addr(k_full + st), (j / kPfStages) & 1) &&
-               (j < 2 || mbar_wait_bounded(smem_addr(s_free + b), ((j >> 1) - 1) & 1));
-          if (!ok || *abort_flag) break;
-          tc_fence_after();
-          const uint32_t kst = sKV + 2 * st * kKVBytes;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t c = k / 4, kk = k % 4;
-            umma_f16(tS + 64 * b, umma_sdesc(sQ + c * kQRegion + kk * 32, 16, 1024),
-                     umma_sdesc(kst + c * kKVRegion + kk * 32, 16, 1024), idS, k > 0);
-          }
-          umma_commit(smem_addr(s_full + b));
-          umma_commit(smem_addr(k_empty + st));
+      int ns = 0, npv = 0;
+      uint32_t idle = 0;
+      unsigned long long idle_since = 0;
+      while (npv < ntiles) {
+        if (*abort_flag) {
+          ok = false;
+          break;
         }
-        if (j >= 1) {
-          const int jp = j - 1, stp = jp % kPfStages;
-          ok = mbar_wait_bounded(smem_addr(p_full), jp & 1) &&
-               mbar_wait_bounded(smem_addr(v_full + stp), (jp / kPfStages) & 1);
-          if (!ok || *abort_flag) break;
-          tc_fence_after();
-          const uint32_t vst = sKV + 2 * stp * kKVBytes + kKVBytes;
+        bool did = false;
+        if (ns < ntiles) {
+          const int st = ns % kPfStages, b = ns & 1;
+          if (mbar_test(smem_addr(k_full + st), (ns / kPfStages) & 1) &&
+              (ns < 2 || mbar_test(smem_addr(s_free + b), ((ns >> 1) - 1) & 1))) {
+            tc_fence_after();
+            const uint32_t kst = sKV + 2 * st * kKVBytes;
 #pragma unroll
-          for (int k = 0; k < kPfKeys / 16; ++k)
-            umma_f16(tO, umma_sdesc(sP + k * 32, 16, 1024),
-                     umma_sdesc(vst + k * 16 * 128, kKVRegion, 1024), idO, jp > 0 || k > 0);
-          umma_commit(smem_addr(o_done));
-          umma_commit(smem_addr(v_empty + stp));
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t c = k / 4, kk = k % 4;
+              umma_f16(tS + 64 * b, umma_sdesc(sQ + c * kQRegion + kk * 32, 16, 1024),
+                       umma_sdesc(kst + c * kKVRegion + kk * 32, 16, 1024), idS, k > 0);
+            }
+            umma_commit(smem_addr(s_full + b));
+            umma_commit(smem_addr(k_empty + st));
+            ++ns;
+            did = true;
+          }
+        }
+        if (npv < ns) {
+          const int stp = npv % kPfStages;
+          if (mbar_test(smem_addr(p_full), npv & 1) &&
+              mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1)) {
+            tc_fence_after();
+            const uint32_t vst = sKV + 2 * stp * kKVBytes + kKVBytes;
+#pragma unroll
+            for (int k = 0; k < kPfKeys / 16; ++k)
+              umma_f16(tO, umma_sdesc(sP + k * 32, 16, 1024),
+                       umma_sdesc(vst + k * 16 * 128, kKVRegion, 1024), idO, npv > 0 || k > 0);
+            umma_commit(smem_addr(o_done));
+            umma_commit(smem_addr(v_empty + stp));
+            ++npv;
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if (idle++ == 0) {
+          idle_since = global_ns();
+        } else if ((idle & 63u) == 0 && global_ns() - idle_since > kWaitLimitNs) {
+          ok = false;
+          break;
         }
       }
       if (!ok) {
