@@ -92,3 +92,20 @@ def test_prefill_host_validation():
     with pytest.raises(pa.PaError) as e:
         pa.pa_prefill(q, case.k_pool, case.v_pool, case.block_tables, case.ctx_lens, qs, 0.125)
     assert e.value.status == pa.PA_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("group,n", [(4, 20), (4, 33), (1, 129), (16, 9), (8, 17)])
+def test_prefill_tile_edges(group, n):
+    """Chunks that end just inside or just past a 128-row query tile (128 / G tokens)."""
+    hkv = 2
+    spec = synth.DecodeSpec(f"pf_edge_g{group}", 2, hkv * group, hkv, 128, 16, "bf16", "bf16",
+                            ctx_lens=(n + 37, n))
+    case = synth.make_case(spec, seed=90 + group)
+    qs = torch.tensor([0, n, 2 * n], dtype=torch.int32)
+    q = torch.randn(2 * n, hkv * group, 128, generator=torch.Generator().manual_seed(n)).to(torch.bfloat16)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qs.cuda(),
+                        case.scale)
+    torch.cuda.synchronize()
+    assert _err(out, ref) <= TOL["bf16"]
