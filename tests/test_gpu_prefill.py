@@ -109,3 +109,20 @@ def test_prefill_tile_edges(group, n):
                         case.scale)
     torch.cuda.synchronize()
     assert _err(out, ref) <= TOL["bf16"]
+
+
+def test_prefill_permutation_invariant_bitwise():
+    """Moving blocks around the pool changes nothing, bit for bit (summary page, block table):
+    the key tiles are gathered in logical order whatever their physical place."""
+    spec = synth.DecodeSpec("pf_perm", 5, 32, 8, 128, 16, "bf16", "bf16", ctx_range=(100, 700))
+    case = synth.make_case(spec, seed=123)
+    qs, q = synth.prefill_queries(case, seed=4)
+    qd, qsd = q.cuda(), qs.cuda()
+
+    def run(c):
+        g = c.to("cuda")
+        return pa.pa_prefill(qd, g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qsd, c.scale)
+
+    ref = run(case)
+    for seed in (1, 2, 3):
+        assert torch.equal(run(synth.permuted(case, seed)), ref)
