@@ -360,19 +360,7 @@ def run_ours(args, world, rank, local) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded block pools shaped like the pages' workloads)",
-        "config": {
-            "workload": (f"{args.workload}: {spec.num_seqs} seqs, {spec.num_q_heads} q / "
-                         f"{spec.num_kv_heads} kv heads x {spec.head_dim}, {spec.kv_dtype} KV, "
-                         f"block {spec.block_size}, ctx U{list(spec.ctx_range)} (>= "
-                         f"{spec.shared_prompt + 1}), {spec.num_seqs // spec.group_size} groups x "
-                         f"{spec.group_size} share a {spec.shared_prompt}-token prompt, "
-                         f"{case.cow_pairs.shape[0]} CoW copies/step, 1 layer"),
-            "step": "pa_write_kv + pa_copy_blocks + pa_decode (split-K combine in-kernel), "
-                    "replayed from a CUDA graph",
-            "split_tokens": split, "num_blocks": case.num_blocks,
-            "ctx_tokens": int(case.ctx_lens.sum()), "l2": "flushed between steps (untimed); "
-            "pool larger than L2", "parallelism": f"replicas x{world}",
-        },
+        "config": workload_config(args.workload, spec, case, split, world),
         "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 1),
         "decode_tokens_per_s": round(world * spec.num_seqs / (ms_per_step * 1e-3), 1),
         "ms_per_step_eager": round(eager_ms, 4),
@@ -798,19 +786,39 @@ def cpu_baseline(case: synth.PagedCase, split: int, seconds: float) -> dict:
                       f"sequences (seeded order), logical KV bytes per second"}
 
 
+def workload_config(name: str, spec: synth.DecodeSpec, case: synth.PagedCase, split: int,
+                    world: int) -> dict:
+    """The `config` object of both arms' JSON lines."""
+    return {
+        "workload": (f"{name}: {spec.num_seqs} seqs, {spec.num_q_heads} q / "
+                     f"{spec.num_kv_heads} kv heads x {spec.head_dim}, {spec.kv_dtype} KV, "
+                     f"block {spec.block_size}, ctx U{list(spec.ctx_range)} (>= "
+                     f"{spec.shared_prompt + 1}), {spec.num_seqs // spec.group_size} groups x "
+                     f"{spec.group_size} share a {spec.shared_prompt}-token prompt, "
+                     f"{case.cow_pairs.shape[0]} CoW copies/step, 1 layer"),
+        "step": "pa_write_kv + pa_copy_blocks + pa_decode (split-K combine in-kernel), "
+                "replayed from a CUDA graph",
+        "split_tokens": split, "num_blocks": case.num_blocks,
+        "ctx_tokens": int(case.ctx_lens.sum()), "l2": "flushed between steps (untimed); "
+        "pool larger than L2", "parallelism": f"replicas x{world}",
+    }
+
+
 def run_reference(args, world, rank) -> None:
-    """Reference arm: the CPU oracle timed on a bounded sample of the same workload."""
+    """Reference arm: the CPU oracle timed on a bounded sample of the same workload. The
+    sample (sequences per step) is sized from a short calibration so that the whole run of
+    warm-up and timed steps takes about --ref-seconds."""
     if rank != 0:
         return
     import oracle
 
     spec = synth.SPECS[args.workload]
     case = synth.make_case(spec, seed=SEED, device="cpu", logical=False, poison=False)
+    split = args.split_tokens or split_tokens_for(spec)
     orc = oracle.load()
     kp = case.k_pool.view(torch.uint8).numpy().reshape(-1).copy()
     vp = case.v_pool.view(torch.uint8).numpy().reshape(-1).copy()
     rng = np.random.default_rng(SEED)
-    sample = 8
     row = spec.num_kv_heads * spec.head_dim * synth.ELT_BYTES[spec.kv_dtype]
 
     def one(seqs):
@@ -824,6 +832,11 @@ def run_reference(args, world, rank) -> None:
                    block_size=spec.block_size, scale=case.scale)
         return 2 * row * int(case.ctx_lens[idx].sum()) + 4 * len(seqs) * row
 
+    t0 = time.perf_counter()
+    one(rng.choice(spec.num_seqs, 2, replace=False))
+    per_seq = (time.perf_counter() - t0) / 2
+    per_step = args.ref_seconds / max(1, args.steps + args.warmup)
+    sample = int(min(spec.num_seqs, max(1, per_step // max(per_seq, 1e-9))))
     for _ in range(args.warmup):
         one(rng.choice(spec.num_seqs, sample, replace=False))
     t0 = time.perf_counter()
@@ -837,10 +850,12 @@ def run_reference(args, world, rank) -> None:
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * el / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload} (sample of {sample} sequences per step)"},
+        "config": workload_config(args.workload, spec, case, split, world),
         "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": orc.max_threads(),
                          "kind": "oracle",
-                         "sample": f"{sample} seeded sequences per step: write_kv + decode"},
+                         "sample": f"{sample} of {spec.num_seqs} seeded sequences per step "
+                                   f"(sized for ~{args.ref_seconds:g} s in all): write_kv + "
+                                   f"decode, KV bytes read per second"},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -859,6 +874,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="time budget of the reference arm's warm-up and timed steps")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
