@@ -95,7 +95,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_q_heads;
 
-  if (n > L || L > p.max_blocks * p.block_size) {  // invalid lengths: zero rows, flag
+  // invalid lengths (or a chunk longer than the grid's max_q_len): zero rows, flag
+  if (n > L || L > p.max_blocks * p.block_size || n > static_cast<int>(gridDim.x) * kTokens) {
     if (tid == 0) flag_error(p.err, kErrCtxLen);
     for (int idx = tid; idx < kPfRows * (D / 8); idx += kPfThreads) {
       const int r = idx / (D / 8), c8 = idx % (D / 8), t = t0 + r / G;

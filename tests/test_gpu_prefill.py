@@ -126,3 +126,22 @@ def test_prefill_permutation_invariant_bitwise():
     ref = run(case)
     for seed in (1, 2, 3):
         assert torch.equal(run(synth.permuted(case, seed)), ref)
+
+
+def test_prefill_chunk_longer_than_max_q_len_flagged():
+    """A chunk longer than the max_q_len the grid was sized with is an error, not a silently
+    half-written output: the flag is set and the rows the grid covers are zero."""
+    spec = synth.DecodeSpec("pf_maxq", 2, 8, 2, 128, 16, "bf16", "bf16", ctx_lens=(300, 90))
+    case = synth.make_case(spec, seed=6).to("cuda")
+    qs = torch.tensor([0, 300, 390], dtype=torch.int32, device="cuda")
+    q = torch.randn(390, 8, 128, device="cuda").to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(q, 7.0)
+    pa.pa_prefill(q, case.k_pool, case.v_pool, case.block_tables, case.ctx_lens, qs, case.scale,
+                  out=out, max_q_len=100, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_ERR_CTX_LEN
+    covered = 128 // 4 * ((100 + 31) // 32)  # tokens per 128-row tile (G = 4) x tiles
+    assert torch.count_nonzero(out[:covered]).item() == 0
+    ref = _oracle(case, qs.cpu(), q.cpu())
+    assert _err(out[300:], ref[300:]) <= TOL["bf16"]  # the other sequence is unaffected
