@@ -58,7 +58,8 @@ def test_scheduler_drives_the_kernels(mode):
     cpu_pool = torch.zeros(ncpu, 1, 2, HKV * B * D * 2, dtype=torch.uint8).pin_memory()
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     orc = oracle.load()
-    seen = {"preempted": 0, "copies": 0, "swap": 0}
+    seen = {"preempted": 0, "copies": 0, "swap": 0, "prefills": 0, "recomputes": 0}
+    preempted_ids = set()
     step = 0
     while step < 400:
         for r, p, m, n, at in reqs:
@@ -66,6 +67,7 @@ def test_scheduler_drives_the_kernels(mode):
                 assert s.add_request(r, p, m, n)
         plan = s.step()
         seen["preempted"] += len(plan.preempted)
+        preempted_ids.update(int(x) for x in plan.preempted)
         seen["copies"] += len(plan.copies)
         seen["swap"] += len(plan.swap_out) + len(plan.swap_in)
         sch.execute_moves(plan, [kp], [vp], cpu_pool, err_flag=err)
@@ -75,6 +77,32 @@ def test_scheduler_drives_the_kernels(mode):
             rows = torch.from_numpy(_identity_rows(wseq, plan.write_pos_np.astype(np.int64), prompts))
             pa.pa_write_kv(k_rows_d[rows.to(dev)].contiguous(), v_rows_d[rows.to(dev)].contiguous(),
                            kp, vp, torch.from_numpy(plan.slots_np).to(dev), err_flag=err)
+        # sequences whose whole context is written this step (an admitted prompt, or a recomputed
+        # victim's prompt and generated tokens) are prefilled: causal attention of all their
+        # positions over the pool, through pa_prefill, against the oracle
+        full = []
+        if len(plan.slots_np):
+            for j in np.unique(plan.write_seq_np):
+                pos = plan.write_pos_np[plan.write_seq_np == j]
+                if pos.min() == 0 and len(pos) == int(plan.ctx_np[j]):
+                    full.append(int(j))
+        if full:
+            lens = [int(plan.ctx_np[j]) for j in full]
+            qs = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32))
+            qq = torch.randn(int(qs[-1]), HQ, D, generator=g).to(torch.float16)
+            bt = torch.from_numpy(np.ascontiguousarray(plan.tables_np[full]))
+            cl = torch.from_numpy(np.ascontiguousarray(plan.ctx_np[full]))
+            pout = pa.pa_prefill(qq.to(dev), kp, vp, bt.to(dev), cl.to(dev), qs.to(dev), 0.125,
+                                 err_flag=err)
+            torch.cuda.synchronize()
+            assert int(err.item()) == 0, step
+            ref = orc.prefill(qq, kp.cpu(), vp.cpu(), bt, cl, qs, dtype="f16", num_q_heads=HQ,
+                              num_kv_heads=HKV, head_dim=D, block_size=B, scale=0.125)
+            e = float(np.abs(pout.double().cpu().numpy() - ref).max())
+            assert e <= TOL["f16"], (step, e)
+            seen["prefills"] += len(full)
+            # preempted lists request ids; a sequence id is request * 256 + sample
+            seen["recomputes"] += sum(int(ids[j]) // 256 in preempted_ids for j in full)
         if len(ids):
             q = torch.randn(len(ids), HQ, D, generator=g).to(torch.float16)
             bt = torch.from_numpy(plan.tables_np).to(dev)
@@ -105,6 +133,8 @@ def test_scheduler_drives_the_kernels(mode):
         if step > 40 and not s.has_unfinished():
             break
     assert not s.has_unfinished(), "the run did not finish"
-    assert seen["preempted"] > 0, seen
+    assert seen["preempted"] > 0 and seen["prefills"] > 0, seen
+    if mode == sch.RECOMPUTE:
+        assert seen["recomputes"] > 0, seen  # a preempted victim came back through pa_prefill
     if mode == sch.SWAP:
         assert seen["copies"] > 0 and seen["swap"] > 0, seen
