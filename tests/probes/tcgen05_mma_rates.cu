@@ -9,11 +9,13 @@
 //   1  M128 N128 K16, A and B K-major in shared memory
 //   2  M128 N128 K16, A from tensor memory, B MN-major in shared memory (a PV step)
 //   3  M128 N256 K16, A and B K-major in shared memory
-//   4  attention order over 64-key tiles for two query tiles: S_0, S_1 (8 MMAs each, N64, into
-//      S buffer j % 2), then PV_0, PV_1 (4 MMAs each, N128, P read from the other S buffer)
-//   5  mode 4 with one commit after the S pair and one after the PV pair
-//   6  attention order over 128-key tiles (every MMA N128: 8 S and 8 PV per query tile) with
-//      one commit after the S pair and one after the PV pair
+//   4  one query tile: S (8 MMAs, N64, shared-memory operands) then PV (4 MMAs, N128, B MN-major,
+//      another accumulator), alternating: accumulator, N and B major all change between groups
+//   5  attention order over 64-key tiles for two query tiles: S_0, S_1 (8 MMAs each, N64), then
+//      PV_0, PV_1 (4 MMAs each, N128, P from shared memory); each S_x at a fixed column
+//   6  mode 5 with S_x double-buffered at columns c and c + 64 (one 128-column group), the
+//      buffer alternating tile by tile
+//   7  mode 6 with one commit after the S pair and one after the PV pair
 // Every wait is bounded; a timeout is reported as status 1.
 #include <cuda_runtime.h>
 
@@ -69,7 +71,7 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   }
 }
 
-constexpr int kMmas = 672;  // a multiple of 24 and of 32 (whole tiles in modes 4-6)
+constexpr int kMmas = 672;  // a multiple of 12 and of 24 (whole groups in modes 4-7)
 
 template <int MODE>
 __global__ void rates(long long* out, int* status) {
@@ -106,25 +108,22 @@ __global__ void rates(long long* out, int* status) {
         mma_ts(t, t + 256 + k * 8, desc(b + k * 2048, 8192, 1024), idesc(128, 128, 1));
       } else if (MODE == 3) {
         mma_ss(t + 256, desc(a + k * 32, 16, 1024), desc(b + k * 32, 16, 1024), idesc(128, 256, 0));
-      } else if (MODE == 4 || MODE == 5) {
+      } else if (MODE == 4) {
+        if (i % 12 < 8)
+          mma_ss(t + 256, desc(a + k * 32, 16, 1024), desc(b + k * 32, 16, 1024), idesc(128, 64, 0));
+        else
+          mma_ss(t, desc(a + 16384 + k * 32, 16, 1024), desc(b + k * 2048, 8192, 1024),
+                 idesc(128, 128, 1));
+      } else {
         const int ph = i % 24, tile = i / 24;
-        const uint32_t sbuf = 64u * (tile & 1), pbuf = 64u * ((tile + 1) & 1);
+        const uint32_t sbuf = MODE == 5 ? 0u : 64u * (tile & 1);
         if (ph < 16)
           mma_ss(t + 256 + (ph >= 8 ? 128u : 0u) + sbuf, desc(a + k * 32, 16, 1024),
                  desc(b + k * 32, 16, 1024), idesc(128, 64, 0));
         else
-          mma_ts(t + (ph >= 20 ? 128u : 0u), t + 256 + (ph >= 20 ? 128u : 0u) + pbuf + k * 8,
+          mma_ss(t + (ph >= 20 ? 128u : 0u), desc(a + 16384 + k * 32, 16, 1024),
                  desc(b + k * 2048, 8192, 1024), idesc(128, 128, 1));
-        if (MODE == 5 && (ph == 15 || ph == 23)) commit(saddr(&groups));
-      } else {
-        const int ph = i % 32;
-        if (ph < 16)
-          mma_ss(t + 256 + (ph >= 8 ? 128u : 0u), desc(a + k * 32, 16, 1024),
-                 desc(b + k * 32, 16, 1024), idesc(128, 128, 0));
-        else
-          mma_ts(t + (ph >= 24 ? 128u : 0u), t + 256 + (ph >= 24 ? 128u : 0u) + (ph & 7) * 8,
-                 desc(b + k * 2048, 8192, 1024), idesc(128, 128, 1));
-        if (ph == 15 || ph == 31) commit(saddr(&groups));
+        if (MODE == 7 && (ph == 15 || ph == 23)) commit(saddr(&groups));
       }
     }
     const long long c1 = clock64();
@@ -156,14 +155,15 @@ int main() {
   long long* d = nullptr;
   int* st = nullptr;
   if (cudaMalloc(&d, 16) != cudaSuccess || cudaMalloc(&st, 4) != cudaSuccess) return 2;
-  const char* names[7] = {"N64 smem A", "N128 smem A", "N128 tmem A (PV)", "N256 smem A",
-                          "attention 64-key tiles", "attention 64-key tiles, commits",
-                          "attention 128-key tiles, commits"};
+  const char* names[8] = {"N64 smem A", "N128 smem A", "N128 tmem A (PV)", "N256 smem A",
+                          "S / PV alternating, one query tile", "attention, S at fixed columns",
+                          "attention, S double-buffered in one 128-column group",
+                          "attention, S double-buffered, commits"};
   // flops per MMA averaged over the mode's sequence
   const double f64 = 128.0 * 64 * 16 * 2, f128 = 128.0 * 128 * 16 * 2;
-  const double flops[7] = {f64, f128, f128, 2 * f128, (16 * f64 + 8 * f128) / 24,
-                           (16 * f64 + 8 * f128) / 24, f128};
-  for (int mode = 0; mode < 7; ++mode) {
+  const double mix = (16 * f64 + 8 * f128) / 24;
+  const double flops[8] = {f64, f128, f128, 2 * f128, (8 * f64 + 4 * f128) / 12, mix, mix, mix};
+  for (int mode = 0; mode < 8; ++mode) {
     long long h[2] = {0, 0};
     int hs = 0;
     for (int rep = 0; rep < 3; ++rep) {  // the last of three runs is reported
@@ -176,7 +176,8 @@ int main() {
         case 3: e = launch<3>(d, st); break;
         case 4: e = launch<4>(d, st); break;
         case 5: e = launch<5>(d, st); break;
-        default: e = launch<6>(d, st); break;
+        case 6: e = launch<6>(d, st); break;
+        default: e = launch<7>(d, st); break;
       }
       if (e == cudaSuccess) e = cudaDeviceSynchronize();
       if (e != cudaSuccess) {
