@@ -138,16 +138,20 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   const int nkeys = L - n + t_last + 1;
   const int ntiles = (nkeys + kPfKeys - 1) / kPfKeys;
 
-  // Q tile -> shared memory, swizzled K-major; rows past the chunk are zero
-  for (int idx = tid; idx < kPfRows * (D / 8); idx += kPfThreads) {
+  // Q tile -> shared memory, swizzled K-major; rows past the chunk are zero. Every load of a
+  // thread is issued before its first store (one memory latency, not one per load), and the
+  // loads are in flight while the barriers and tensor memory are set up.
+  constexpr int kQLoads = kPfRows * (D / 8) / kPfThreads;  // 16-byte loads per thread
+  static_assert(kPfRows * (D / 8) % kPfThreads == 0, "the Q tile splits evenly over the threads");
+  uint4 qv[kQLoads];
+#pragma unroll
+  for (int i = 0; i < kQLoads; ++i) {
+    const int idx = tid + i * kPfThreads;
     const int r = idx / (D / 8), c8 = idx % (D / 8), t = t0 + r / G;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (t < n)
-      v = __ldg(reinterpret_cast<const uint4*>(
-                    p.q + (static_cast<size_t>(q0 + t) * Hq + g * G + r % G) * D) + c8);
-    *reinterpret_cast<uint4*>(bp + (c8 / 8) * kQRegion + sw128_offset(r, c8 % 8)) = v;
+    qv[i] = t < n ? __ldg(reinterpret_cast<const uint4*>(
+                              p.q + (static_cast<size_t>(q0 + t) * Hq + g * G + r % G) * D) + c8)
+                  : make_uint4(0, 0, 0, 0);
   }
-  fence_proxy_async_smem();
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < kPfStages; ++i) {
@@ -166,6 +170,13 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+#pragma unroll
+  for (int i = 0; i < kQLoads; ++i) {
+    const int idx = tid + i * kPfThreads;
+    const int r = idx / (D / 8), c8 = idx % (D / 8);
+    *reinterpret_cast<uint4*>(bp + (c8 / 8) * kQRegion + sw128_offset(r, c8 % 8)) = qv[i];
+  }
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
