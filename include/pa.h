@@ -159,6 +159,10 @@ pa_status pa_decode(const pa_decode_args* args, pa_stream stream);
  * written); an out-of-pool block id sets PA_ERR_BLOCK_ID (those rows are then unspecified).
  * Supported: dtype PA_F16 or PA_BF16 (q, K/V and out alike); head_dim 64 or 128; block_size 8,
  * 16, 32 or 64; group size 1, 2, 4, 8 or 16.
+ * The kernel is persistent (two CTAs per SM). With work_counter set, the call zeroes that int32
+ * on the stream and the CTAs take work items from it, longest first within each (sequence, kv
+ * head); NULL assigns the items round-robin. The counter must not be shared by calls that can
+ * run at the same time.
  */
 typedef struct {
   const void* q;
@@ -180,6 +184,7 @@ typedef struct {
   pa_dtype dtype;
   float scale;
   int32_t* err_flag;     /* device int32 or NULL */
+  int32_t* work_counter; /* device int32 or NULL, see above */
 } pa_prefill_args;
 
 pa_status pa_prefill(const pa_prefill_args* args, pa_stream stream);

@@ -69,6 +69,34 @@ pa_status encode_pool_rows_map(CUtensorMap* map, const void* pool, long long row
   return PA_OK;
 }
 
+// Queries [num_tokens][num_q_heads][head_dim] (16-bit) as a 3-D tensor {head_dim, num_q_heads,
+// num_tokens} with a box of {64, group, tokens} and 128-byte swizzle: one box lands as
+// tokens * group rows of 128 bytes, row t * group + h holding head h of token t, the layout of a
+// 2-D box of as many rows (tokens past num_tokens read as zero).
+pa_status encode_query_tile_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads,
+                                int head_dim, int group, int tokens, std::string& msg) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) {
+    msg = "cuTensorMapEncodeTiled is not available from the driver";
+    return PA_ECUDA;
+  }
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_q_heads),
+                        static_cast<cuuint64_t>(num_tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                           static_cast<cuuint64_t>(num_q_heads) * head_dim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tokens)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    msg = "cuTensorMapEncodeTiled (queries) failed with CUresult " +
+          std::to_string(static_cast<int>(r));
+    return PA_ECUDA;
+  }
+  return PA_OK;
+}
+
 pa_status cuda_status(cudaError_t e, const char* what, std::string& msg) {
   if (e == cudaSuccess) return PA_OK;
   msg = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";

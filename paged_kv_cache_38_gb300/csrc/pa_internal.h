@@ -75,6 +75,8 @@ pa_status run_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t nu
 pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string& msg);
 pa_status encode_pool_rows_map(CUtensorMap* map, const void* pool, long long rows, int head_dim,
                                int elt, int box_rows, std::string& msg);
+pa_status encode_query_tile_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads,
+                                int head_dim, int group, int tokens, std::string& msg);
 pa_status record_error(pa_status st, const std::string& msg);
 
 // Sets msg from a CUDA error and returns PA_ECUDA (or PA_OK for cudaSuccess).

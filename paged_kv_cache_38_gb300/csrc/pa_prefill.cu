@@ -6,21 +6,27 @@
 // together). Query i of a chunk of n tokens over a cache of L positions stands at position
 // L - n + i and attends to positions 0 .. L - n + i.
 //
-// GB300 design: one CTA per (sequence, kv head, tile of 128 query rows); a row is one (token,
-// query head of the group), so a tile holds 128 / G tokens and the GQA group shares every K/V
-// tile. K/V tiles of 64 keys stream through a 2-stage shared-memory ring (about 113 KB per CTA
-// at head_dim 128, so two CTAs share an SM and overlap each other's softmax and MMA phases):
-//   * warps 0 and 2 issue 2-D TMA copies of the K and the V tiles through the block table
-//     (copy units of min(block_size, 64) rows, 128-byte swizzle), each through its own ring;
+// GB300 design: a persistent kernel, two CTAs per SM (about 113 KB of shared memory and 256
+// tensor-memory columns each at head_dim 128, so the two overlap each other's softmax and MMA
+// phases). A work item is one tile of 128 query rows of one (sequence, kv head); a row is one
+// (token, query head of the group), so a tile holds 128 / G tokens and the GQA group shares
+// every K/V tile. Items are taken longest first within each (sequence, kv head), from a work
+// counter or round-robin; tensor memory, barriers and the K/V rings live across items, so the
+// next item's queries and first K/V tiles load while the current one finishes. Roles:
+//   * warp 3 takes items and publishes them through a 2-slot ring; it loads each item's query
+//     tile (one 3-D TMA box per 64 columns) once the previous item's last S MMA has completed;
+//   * warps 0 and 2 issue 2-D TMA copies of the K and the V tiles (64 keys) through the block
+//     table (copy units of min(block_size, 64) rows, 128-byte swizzle), each through its own
+//     2-stage ring;
 //   * warp 1 allocates tensor memory and one lane issues the MMAs: S_j = Q K_j^T (M 128, N 64)
-//     into one of two TMEM S buffers, and O += P_{j-1} V_{j-1} (M 128, N = head_dim) into the
-//     TMEM O accumulator, each completion signalled by tcgen05.commit on an mbarrier;
+//     into one of two TMEM S buffers, and O += P_j V_j (M 128, N = head_dim) into the TMEM O
+//     accumulator, each completion signalled by tcgen05.commit on an mbarrier;
 //   * warps 4-7 (one thread per row) read S with tcgen05.ld, apply the causal mask and the
 //     online softmax (log2 domain), write P (16-bit, swizzled K-major) to shared memory and
-//     rescale O in tensor memory when a row's running maximum grows; at the end they divide O
-//     by the row sums and store the output.
-// Every wait is bounded; on a timeout the CTA flags PA_ERR_TIMEOUT, drains its MMAs through one
-// last commit and frees its tensor memory before it returns.
+//     rescale O in tensor memory when a row's running maximum grows; at the end of an item they
+//     divide O by the row sums and store the rows.
+// Every wait is bounded; on a timeout the CTA flags PA_ERR_TIMEOUT, the roles wind down, the
+// MMAs drain through one last commit and the tensor memory is freed before the CTA returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,19 +47,29 @@ constexpr int kPfThreads = 256;   // 8 warps
 constexpr int kPfRows = 128;      // query rows per tile = MMA M
 constexpr int kPfKeys = 64;       // keys per K/V tile: S columns, PV reduction
 constexpr int kPfStages = 2;      // K/V ring depth (two CTAs fit on an SM)
+constexpr int kSlots = 2;         // published work items
 constexpr int kSoftmaxWarp0 = 4;  // warps 4..7 form the softmax warpgroup
+constexpr int kItemReaders = 3 + 4;  // K producer, V producer, MMA issuer, 4 softmax warps
 constexpr uint32_t kTmemCols = 256;  // O at columns [0, head_dim), S buffers at [128, 192), [192, 256)
+constexpr uint32_t kCtlBytes = 384;  // barriers, item slots, tensor-memory address, abort flag
 
 struct PrefillParams {
-  const uint16_t* q;
   void* out;
   const int32_t* block_tables;
   const int32_t* ctx_lens;
   const int32_t* q_starts;
   int32_t* err;
-  int num_q_heads, num_kv_heads, block_size, log2_block, num_blocks, max_blocks;
+  int32_t* work;  // work counter, or null for round-robin items
+  int num_tokens, num_q_heads, num_kv_heads, block_size, log2_block, num_blocks, max_blocks;
   int log2_urows;    // rows per K/V copy: min(block_size, 64)
+  int tiles;         // query tiles per (sequence, kv head) at the longest chunk (max_q_len)
+  int total;         // num_seqs * num_kv_heads * tiles
   float scale_log2;  // scale * log2(e)
+};
+
+// A published work item; s < 0 ends the work.
+struct PfItem {
+  int s, g, t0, n, L, q0, ntiles, pad;
 };
 
 // 16 fp32 values as 8 packed 16-bit pairs in memory order.
@@ -68,18 +84,10 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   }
 }
 
-template <bool BF16>
-__device__ __forceinline__ float2 unpack16(uint32_t u) {
-  if constexpr (BF16) {
-    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-  } else {
-    return __half22float2(*reinterpret_cast<const __half2*>(&u));
-  }
-}
-
 template <int D, int G, bool BF16>
 __global__ void __launch_bounds__(kPfThreads, 2)
-    pa_prefill_kernel(const __grid_constant__ CUtensorMap kmap,
+    pa_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillParams p) {
   constexpr int kRegions = D / 64;
   constexpr int kTokens = kPfRows / G;
@@ -87,26 +95,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   constexpr uint32_t kKVRegion = kPfKeys * 128;       // 8 KiB
   constexpr uint32_t kKVBytes = kRegions * kKVRegion;  // K (or V) of one stage
 
-  const int s = blockIdx.z, g = blockIdx.y, t0 = blockIdx.x * kTokens;
-  const int q0 = __ldg(p.q_starts + s);
-  const int n = __ldg(p.q_starts + s + 1) - q0;
-  if (t0 >= n) return;  // the whole CTA: no query of this tile
-  const int L = __ldg(p.ctx_lens + s);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hq = p.num_q_heads;
-
-  // invalid lengths (or a chunk longer than the grid's max_q_len): zero rows, flag
-  if (n > L || L > p.max_blocks * p.block_size || n > static_cast<int>(gridDim.x) * kTokens) {
-    if (tid == 0) flag_error(p.err, kErrCtxLen);
-    for (int idx = tid; idx < kPfRows * (D / 8); idx += kPfThreads) {
-      const int r = idx / (D / 8), c8 = idx % (D / 8), t = t0 + r / G;
-      if (t < n)
-        reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                 (static_cast<size_t>(q0 + t) * Hq + g * G + r % G) * D)[c8] =
-            make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_addr(smem_raw);
@@ -118,40 +108,28 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   const uint32_t sQ = base;
   const uint32_t sKV = sQ + kRegions * kQRegion;  // stage st: K at sKV + 2 st kKVBytes, V after it
   const uint32_t sP = sKV + kPfStages * 2 * kKVBytes;
-  uint8_t* bars_p = bp + (sP - base) + kPfRows * 128;
+  uint8_t* ctl = bp + (sP - base) + kPfRows * 128;
   // K and V stream through separate rings: K of tile j is free once S_j is computed, V once
-  // PV_j is, so K loads run a whole softmax ahead of V loads.
-  uint64_t* k_full = reinterpret_cast<uint64_t*>(bars_p);  // [kPfStages]
-  uint64_t* k_empty = k_full + kPfStages;                   // [kPfStages]
-  uint64_t* v_full = k_empty + kPfStages;                   // [kPfStages]
-  uint64_t* v_empty = v_full + kPfStages;                   // [kPfStages]
-  uint64_t* s_full = v_empty + kPfStages;                   // [2]
-  uint64_t* s_free = s_full + 2;                             // [2]
+  // PV_j is, so K loads run a whole softmax ahead of V loads. Every phase below counts tiles
+  // (or items) over the whole run of the CTA.
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(ctl);  // [kPfStages]
+  uint64_t* k_empty = k_full + kPfStages;                // [kPfStages]
+  uint64_t* v_full = k_empty + kPfStages;                // [kPfStages]
+  uint64_t* v_empty = v_full + kPfStages;                // [kPfStages]
+  uint64_t* s_full = v_empty + kPfStages;                // [2]
+  uint64_t* s_free = s_full + 2;                         // [2]
   uint64_t* p_full = s_free + 2;
   uint64_t* o_done = p_full + 1;
-  uint64_t* drain = o_done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* o_free = o_done + 1;                         // O read by the epilogue (4 warps)
+  uint64_t* q_full = o_free + 1;                         // the item's query tile landed
+  uint64_t* q_empty = q_full + 1;                        // the item's last S complete
+  uint64_t* item_full = q_empty + 1;                     // [kSlots]
+  uint64_t* item_empty = item_full + kSlots;             // [kSlots]
+  uint64_t* drain = item_empty + kSlots;
+  PfItem* items = reinterpret_cast<PfItem*>(drain + 1);  // [kSlots]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(items + kSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  // causal extent of the tile: its last query stands at position L - n + t_last
-  const int t_last = min(n, t0 + kTokens) - 1;
-  const int nkeys = L - n + t_last + 1;
-  const int ntiles = (nkeys + kPfKeys - 1) / kPfKeys;
-
-  // Q tile -> shared memory, swizzled K-major; rows past the chunk are zero. Every load of a
-  // thread is issued before its first store (one memory latency, not one per load), and the
-  // loads are in flight while the barriers and tensor memory are set up.
-  constexpr int kQLoads = kPfRows * (D / 8) / kPfThreads;  // 16-byte loads per thread
-  static_assert(kPfRows * (D / 8) % kPfThreads == 0, "the Q tile splits evenly over the threads");
-  uint4 qv[kQLoads];
-#pragma unroll
-  for (int i = 0; i < kQLoads; ++i) {
-    const int idx = tid + i * kPfThreads;
-    const int r = idx / (D / 8), c8 = idx % (D / 8), t = t0 + r / G;
-    qv[i] = t < n ? __ldg(reinterpret_cast<const uint4*>(
-                              p.q + (static_cast<size_t>(q0 + t) * Hq + g * G + r % G) * D) + c8)
-                  : make_uint4(0, 0, 0, 0);
-  }
   if (tid == 0) {
     *abort_flag = 0;
     for (int i = 0; i < kPfStages; ++i) {
@@ -166,24 +144,92 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     }
     mbar_init(smem_addr(p_full), 4);
     mbar_init(smem_addr(o_done), 1);
+    mbar_init(smem_addr(o_free), 4);
+    mbar_init(smem_addr(q_full), 1);
+    mbar_init(smem_addr(q_empty), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_addr(item_full + i), 1);
+      mbar_init(smem_addr(item_empty + i), kItemReaders);
+    }
     mbar_init(smem_addr(drain), 1);
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
-#pragma unroll
-  for (int i = 0; i < kQLoads; ++i) {
-    const int idx = tid + i * kPfThreads;
-    const int r = idx / (D / 8), c8 = idx % (D / 8);
-    *reinterpret_cast<uint4*>(bp + (c8 / 8) * kQRegion + sw128_offset(r, c8 % 8)) = qv[i];
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem, tS = tmem + 128;
+  auto fail = [&]() {
+    flag_error(p.err, kErrTimeout);
+    *abort_flag = 1;
+  };
 
-  if (warp == 0 || warp == 2) {
+  if (warp == 3) {
+    // ------------------------------------------------------------------ items and queries
+    if (lane == 0) {
+      prefetch_tensormap(&qmap);
+      const uint64_t qpol = policy_evict_first();  // each query tile is read once
+      int k = 0, fetched = 0;
+      for (;;) {
+        PfItem it{-1, 0, 0, 0, 0, 0, 0, 0};
+        while (!*abort_flag) {
+          const int v = p.work != nullptr
+                            ? atomicAdd(p.work, 1)
+                            : static_cast<int>(blockIdx.x) + fetched * static_cast<int>(gridDim.x);
+          ++fetched;
+          if (v >= p.total) break;
+          const int sg = v / p.tiles;
+          const int tile = p.tiles - 1 - (v - sg * p.tiles);  // longest tile of (s, g) first
+          const int s = sg / p.num_kv_heads, g = sg - s * p.num_kv_heads;
+          const int q0 = __ldg(p.q_starts + s);
+          const int n = __ldg(p.q_starts + s + 1) - q0;
+          const int t0 = tile * kTokens;
+          if (t0 >= n) continue;  // the chunk is shorter than this tile
+          const int L = __ldg(p.ctx_lens + s);
+          const bool rows_ok = q0 >= 0 && q0 + n <= p.num_tokens;
+          // invalid lengths (or a chunk longer than max_q_len): the tile's rows are zero
+          if (!rows_ok || n > L || L > p.max_blocks * p.block_size || n > p.tiles * kTokens) {
+            flag_error(p.err, kErrCtxLen);
+            if (rows_ok) {
+              const int tend = min(n, t0 + kTokens);
+              for (int t = t0; t < tend; ++t)
+                for (int i = 0; i < G * D / 8; ++i)
+                  reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                           (static_cast<size_t>(q0 + t) * Hq + g * G) * D)[i] =
+                      make_uint4(0, 0, 0, 0);
+            }
+            continue;
+          }
+          // causal extent of the tile: its last query stands at position L - n + t_last
+          const int t_last = min(n, t0 + kTokens) - 1;
+          it = PfItem{s, g, t0, n, L, q0, (L - n + t_last + 1 + kPfKeys - 1) / kPfKeys, 0};
+          break;
+        }
+        const int slot = k % kSlots;
+        if (k >= kSlots && !mbar_wait_bounded(smem_addr(item_empty + slot), ((k / kSlots) - 1) & 1)) {
+          fail();
+          it.s = -1;
+        }
+        items[slot] = it;
+        mbar_arrive(smem_addr(item_full + slot));
+        if (it.s < 0) break;
+        // the query buffer is free once the previous item's last S MMA has completed
+        if (k >= 1 && !mbar_wait_bounded(smem_addr(q_empty), (k - 1) & 1)) {
+          fail();
+          break;
+        }
+        mbar_arrive_expect_tx(smem_addr(q_full), kRegions * kQRegion);
+#pragma unroll
+        for (int c = 0; c < kRegions; ++c)
+          tma_load_3d(sQ + c * kQRegion, &qmap, c * 64, it.g * G, it.q0 + it.t0, smem_addr(q_full),
+                      qpol);
+        ++k;
+      }
+      // no query copy may still be landing when the CTA exits (matters after an abort)
+      if (k >= 1) mbar_wait_bounded(smem_addr(q_full), (k - 1) & 1);
+    }
+  } else if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ K/V producers
     // warp 0 streams K, warp 2 streams V, each through its own ring (two lanes of one warp
     // would hold each other up in their barrier waits)
@@ -192,62 +238,75 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       const CUtensorMap* map = is_v ? &vmap : &kmap;
       uint64_t* fullb = is_v ? v_full : k_full;
       uint64_t* emptyb = is_v ? v_empty : k_empty;
-      const int32_t* trow = p.block_tables + static_cast<size_t>(s) * p.max_blocks;
       const uint64_t pol = policy_evict_normal();  // the sequence's other query tiles reread them
       const int urows = 1 << p.log2_urows, B = p.block_size;
       const int units = kPfKeys >> p.log2_urows;
       prefetch_tensormap(map);
-      // The block-table entries of tile j + 1 are read while the producer waits for a free
-      // stage for tile j + 1, so their latency is off the copy path.
-      int ph[8];
-      auto load_phys = [&](int j) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int key = j * kPfKeys + u * urows;
-          ph[u] = (u < units && key < L) ? __ldg(trow + (key >> p.log2_block)) : -2;
-        }
-      };
-      load_phys(0);
-      int issued = 0;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j % kPfStages;
-        if (j >= kPfStages &&
-            !mbar_wait_bounded(smem_addr(emptyb + st), ((j / kPfStages) - 1) & 1)) {
-          flag_error(p.err, kErrTimeout);
-          *abort_flag = 1;
+      int J = 0;  // tiles issued, over all items
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int slot = k % kSlots;
+        if (!mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1)) {
+          fail();
           break;
         }
-        if (*abort_flag) break;
-        int rowc[8];
-        uint32_t bytes = 0;
+        const PfItem it = items[slot];
+        if (it.s < 0 || *abort_flag) break;
+        const int32_t* trow = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks;
+        // The block-table entries of tile j + 1 are read while the producer waits for a free
+        // stage for tile j + 1, so their latency is off the copy path.
+        int ph[8];
+        auto load_phys = [&](int j) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int key = j * kPfKeys + u * urows;
-          rowc[u] = -1;
-          if (ph[u] == -2) continue;  // past the unit count or the cache
-          if (ph[u] < 0 || ph[u] >= p.num_blocks) {
-            if (!is_v) flag_error(p.err, kErrBlockId);
-          } else {
-            rowc[u] = (ph[u] * p.num_kv_heads + g) * B + (key & (B - 1));
-            bytes += static_cast<uint32_t>(kRegions * urows * 128);
+          for (int u = 0; u < 8; ++u) {
+            const int key = j * kPfKeys + u * urows;
+            ph[u] = (u < units && key < it.L) ? __ldg(trow + (key >> p.log2_block)) : -2;
           }
-        }
-        const uint32_t full = smem_addr(fullb + st);
-        mbar_arrive_expect_tx(full, bytes);
-        const uint32_t dst = sKV + 2 * st * kKVBytes + (is_v ? kKVBytes : 0u);
+        };
+        load_phys(0);
+        for (int j = 0; j < it.ntiles; ++j, ++J) {
+          const int st = J % kPfStages;
+          if (J >= kPfStages &&
+              !mbar_wait_bounded(smem_addr(emptyb + st), ((J / kPfStages) - 1) & 1)) {
+            fail();
+            ok = false;
+            break;
+          }
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          int rowc[8];
+          uint32_t bytes = 0;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (rowc[u] < 0) continue;
+          for (int u = 0; u < 8; ++u) {
+            const int key = j * kPfKeys + u * urows;
+            rowc[u] = -1;
+            if (ph[u] == -2) continue;  // past the unit count or the cache
+            if (ph[u] < 0 || ph[u] >= p.num_blocks) {
+              if (!is_v) flag_error(p.err, kErrBlockId);
+            } else {
+              rowc[u] = (ph[u] * p.num_kv_heads + it.g) * B + (key & (B - 1));
+              bytes += static_cast<uint32_t>(kRegions * urows * 128);
+            }
+          }
+          const uint32_t full = smem_addr(fullb + st);
+          mbar_arrive_expect_tx(full, bytes);
+          const uint32_t dst = sKV + 2 * st * kKVBytes + (is_v ? kKVBytes : 0u);
 #pragma unroll
-          for (int c = 0; c < kRegions; ++c)
-            tma_load_2d(dst + c * kKVRegion + static_cast<uint32_t>(u * urows * 128), map, c * 64,
-                        rowc[u], full, pol);
+          for (int u = 0; u < 8; ++u) {
+            if (rowc[u] < 0) continue;
+#pragma unroll
+            for (int c = 0; c < kRegions; ++c)
+              tma_load_2d(dst + c * kKVRegion + static_cast<uint32_t>(u * urows * 128), map,
+                          c * 64, rowc[u], full, pol);
+          }
+          if (j + 1 < it.ntiles) load_phys(j + 1);
         }
-        issued = j + 1;
-        if (j + 1 < ntiles) load_phys(j + 1);
+        if (ok) mbar_arrive(smem_addr(item_empty + slot));
       }
       // no copy of this CTA may still be landing when it exits (matters after an abort)
-      for (int jj = max(0, issued - kPfStages); jj < issued; ++jj)
+      for (int jj = max(0, J - kPfStages); jj < J; ++jj)
         mbar_wait_bounded(smem_addr(fullb + jj % kPfStages), (jj / kPfStages) & 1);
     }
   } else if (warp == 1) {
@@ -255,23 +314,42 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_f16(kPfRows, kPfKeys, BF16, false);
       constexpr uint32_t idO = umma_idesc_f16(kPfRows, D, BF16, true);
-      // Issue S_ns as soon as K_ns has landed (and its S buffer is free), and PV_npv as soon as
-      // P_npv and V_npv are ready, whichever comes first: a late K tile does not hold up the
-      // PV of the previous tile. PVs go in tile order (they accumulate into O).
+      // Two cursors over the items: S_ns is issued as soon as K_ns has landed (and its S buffer
+      // is free, and at an item's first tile its queries have landed), PV_npv as soon as P_npv
+      // and V_npv are ready (and, at an item's first tile, once the epilogue has read O),
+      // whichever comes first. S runs ahead of PV by up to two tiles, across item boundaries.
+      int kS = 0, jS = 0, ns = 0;   // S stream: item, tile in item, S issued over all items
+      bool haveS = false, endS = false;
+      PfItem iS{};
+      int kP = 0, jP = 0, npv = 0;  // PV stream: item, tile in item, PV issued over all items
+      bool haveP = false;
+      PfItem iP{};
+      int nO = 0;  // items whose O is complete
       bool ok = true;
-      int ns = 0, npv = 0;
       uint32_t idle = 0;
       unsigned long long idle_since = 0;
-      while (npv < ntiles) {
+      for (;;) {
         if (*abort_flag) {
           ok = false;
           break;
         }
         bool did = false;
-        if (ns < ntiles) {
+        // ---- S stream
+        if (!haveS && !endS && mbar_test(smem_addr(item_full + kS % kSlots), (kS / kSlots) & 1)) {
+          iS = items[kS % kSlots];
+          if (iS.s < 0) {
+            endS = true;
+          } else {
+            haveS = true;
+            jS = 0;
+          }
+          did = true;
+        }
+        if (haveS) {
           const int st = ns % kPfStages, b = ns & 1;
           if (mbar_test(smem_addr(k_full + st), (ns / kPfStages) & 1) &&
-              (ns < 2 || mbar_test(smem_addr(s_free + b), ((ns >> 1) - 1) & 1))) {
+              (ns < 2 || mbar_test(smem_addr(s_free + b), ((ns >> 1) - 1) & 1)) &&
+              (jS > 0 || mbar_test(smem_addr(q_full), kS & 1))) {
             tc_fence_after();
             const uint32_t kst = sKV + 2 * st * kKVBytes;
 #pragma unroll
@@ -283,22 +361,44 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             umma_commit(smem_addr(s_full + b));
             umma_commit(smem_addr(k_empty + st));
             ++ns;
+            if (++jS == iS.ntiles) {
+              umma_commit(smem_addr(q_empty));
+              haveS = false;
+              ++kS;
+            }
             did = true;
           }
         }
-        if (npv < ns) {
+        // ---- PV stream
+        if (!haveP) {
+          if (kP < kS || (kP == kS && haveS)) {
+            iP = items[kP % kSlots];
+            haveP = true;
+            jP = 0;
+          } else if (endS && kP == kS) {
+            break;  // every item is done
+          }
+        }
+        if (haveP && npv < ns) {
           const int stp = npv % kPfStages;
           if (mbar_test(smem_addr(p_full), npv & 1) &&
-              mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1)) {
+              mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1) &&
+              (jP > 0 || nO == 0 || mbar_test(smem_addr(o_free), (nO - 1) & 1))) {
             tc_fence_after();
             const uint32_t vst = sKV + 2 * stp * kKVBytes + kKVBytes;
 #pragma unroll
             for (int k = 0; k < kPfKeys / 16; ++k)
               umma_f16(tO, umma_sdesc(sP + k * 32, 16, 1024),
-                       umma_sdesc(vst + k * 16 * 128, kKVRegion, 1024), idO, npv > 0 || k > 0);
+                       umma_sdesc(vst + k * 16 * 128, kKVRegion, 1024), idO, jP > 0 || k > 0);
             umma_commit(smem_addr(o_done));
             umma_commit(smem_addr(v_empty + stp));
             ++npv;
+            if (++jP == iP.ntiles) {
+              ++nO;
+              mbar_arrive(smem_addr(item_empty + kP % kSlots));
+              haveP = false;
+              ++kP;
+            }
             did = true;
           }
         }
@@ -311,10 +411,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           break;
         }
       }
-      if (!ok) {
-        flag_error(p.err, kErrTimeout);
-        *abort_flag = 1;
-      }
+      if (!ok) fail();
       // every MMA this thread issued has completed before tensor memory is released
       umma_commit(smem_addr(drain));
       mbar_wait_bounded(smem_addr(drain), 0);
@@ -323,136 +420,149 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     // ------------------------------------------------------------------ softmax warpgroup
     const int r = tid - kSoftmaxWarp0 * 32;  // tile row = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp - kSoftmaxWarp0) * 32) << 16;
-    const int tr = t0 + r / G;
-    const bool row_valid = tr < n;
-    const int pos = L - n + tr;  // last position this row may see
-    float m = -INFINITY, l = 0.f;
+    int jx = 0;  // tiles processed, over all items
     bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      ok = mbar_wait_bounded(smem_addr(s_full + b), (j >> 1) & 1);
+    for (int k = 0;; ++k) {
+      const int slot = k % kSlots;
+      ok = mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1);
       if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      float x[kPfKeys];
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld32_nowait(tS + 64 * b + lane_base, r0);
-        tmem_ld32_nowait(tS + 64 * b + lane_base + 32, r1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(r0[i]);
-          x[32 + i] = __uint_as_float(r1[i]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(s_free + b));
-
-      const int key0 = j * kPfKeys;
-      // Rows that see all 64 keys of the tile (every tile before the diagonal) need no mask.
-      // Scores stay raw until the exponent: m is kept in scaled log2 units and the weight of
-      // score x is 2^(x * scale_log2 - m), one FFMA and one ex2.
-      const bool full = row_valid && key0 + kPfKeys - 1 <= pos;
-      const int lim = row_valid ? pos - key0 : -1;  // last visible column (full: >= 63)
-      float mt = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int c = 0; c < kPfKeys; ++c) mt = fmaxf(mt, x[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < kPfKeys; ++c)
-          if (c <= lim) mt = fmaxf(mt, x[c]);
-      }
-      mt = mt == -INFINITY ? -INFINITY : mt * p.scale_log2;
-      // Lazy rescaling: the row keeps its reference maximum m unless the tile's maximum exceeds
-      // it by more than 8 (log2 units); weights then stay below 2^8 and O is rescaled rarely.
-      // Numerator and denominator share the same reference, so the result is unchanged.
-      const float m_new = mt > m + 8.f ? mt : m;
-      const float alpha = m_new == m ? 1.f : ex2(m - m_new);
-      uint32_t pk[kPfKeys / 2];
-      float psum = 0.f;
-      if (full) {
-#pragma unroll
-        for (int c = 0; c < kPfKeys; c += 2) {
-          const float p0 = ex2(fmaf(x[c], p.scale_log2, -m_new));
-          const float p1 = ex2(fmaf(x[c + 1], p.scale_log2, -m_new));
-          pk[c / 2] = pack16<BF16>(p0, p1);
-          psum += p0 + p1;
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kPfKeys; c += 2) {
-          const float p0 = c <= lim && m_new != -INFINITY ? ex2(fmaf(x[c], p.scale_log2, -m_new)) : 0.f;
-          const float p1 =
-              c + 1 <= lim && m_new != -INFINITY ? ex2(fmaf(x[c + 1], p.scale_log2, -m_new)) : 0.f;
-          pk[c / 2] = pack16<BF16>(p0, p1);
-          psum += p0 + p1;
-        }
-      }
-      l = l * alpha + psum;
-      m = m_new;
-
-      if (j >= 1) {  // PV_{j-1} done: O is stable and the P buffer free
-        ok = mbar_wait_bounded(smem_addr(o_done), (j - 1) & 1);
-        if (__any_sync(0xffffffffu, !ok)) {
+      const PfItem it = items[slot];
+      if (it.s < 0) break;
+      const int tr = it.t0 + r / G;
+      const bool row_valid = tr < it.n;
+      const int pos = it.L - it.n + tr;  // last position this row may see
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.ntiles; ++j, ++jx) {
+        const int b = jx & 1;
+        ok = mbar_wait_bounded(smem_addr(s_full + b), (jx >> 1) & 1);
+        if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
           ok = false;
           break;
         }
         tc_fence_after();
-      }
-      if (j == ntiles - 1 && key0 + kPfKeys > L) {
-        // value rows past the cache's last position (stale slots, or not loaded) become zero,
-        // so that zero weights cannot meet a NaN; the tile's V copies must have landed first
-        ok = mbar_wait_bounded(smem_addr(v_full + (j % kPfStages)), (j / kPfStages) & 1);
-        if (__any_sync(0xffffffffu, !ok)) {
-          ok = false;
-          break;
-        }
-        const uint32_t vst = sKV + 2 * ((ntiles - 1) % kPfStages) * kKVBytes + kKVBytes;
-        const int r0 = L - key0;
-        const int nbytes16 = (kPfKeys - r0) * 8 * kRegions;  // 16-byte chunks to clear
-        for (int i = r; i < nbytes16; i += 128) {
-          const int c = i % (8 * kRegions), row = r0 + i / (8 * kRegions);
-          *reinterpret_cast<uint4*>(bp + (vst - base) + (c / 8) * kKVRegion + row * 128 +
-                                    (c % 8) * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      // P row r, swizzled K-major: 16-byte chunk c holds keys 8c .. 8c + 7
-      uint8_t* prow = bp + (sP - base);
+        float x[kPfKeys];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_nowait(tS + 64 * b + lane_base, r0);
+          tmem_ld32_nowait(tS + 64 * b + lane_base + 32, r1);
+          tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + sw128_offset(r, c)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          for (int i = 0; i < 32; ++i) {
+            x[i] = __uint_as_float(r0[i]);
+            x[32 + i] = __uint_as_float(r1[i]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(s_free + b));
+
+        const int key0 = j * kPfKeys;
+        // Rows that see all 64 keys of the tile (every tile before the diagonal) need no mask.
+        // Scores stay raw until the exponent: m is kept in scaled log2 units and the weight of
+        // score x is 2^(x * scale_log2 - m), one FFMA and one ex2.
+        const bool full = row_valid && key0 + kPfKeys - 1 <= pos;
+        const int lim = row_valid ? pos - key0 : -1;  // last visible column (full: >= 63)
+        float mt = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < kPfKeys; ++c) mt = fmaxf(mt, x[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kPfKeys; ++c)
+            if (c <= lim) mt = fmaxf(mt, x[c]);
+        }
+        mt = mt == -INFINITY ? -INFINITY : mt * p.scale_log2;
+        // Lazy rescaling: the row keeps its reference maximum m unless the tile's maximum
+        // exceeds it by more than 8 (log2 units); weights then stay below 2^8 and O is rescaled
+        // rarely. Numerator and denominator share the same reference, so the result is
+        // unchanged.
+        const float m_new = mt > m + 8.f ? mt : m;
+        const float alpha = m_new == m ? 1.f : ex2(m - m_new);
+        uint32_t pk[kPfKeys / 2];
+        float psum = 0.f;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < kPfKeys; c += 2) {
+            const float p0 = ex2(fmaf(x[c], p.scale_log2, -m_new));
+            const float p1 = ex2(fmaf(x[c + 1], p.scale_log2, -m_new));
+            pk[c / 2] = pack16<BF16>(p0, p1);
+            psum += p0 + p1;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kPfKeys; c += 2) {
+            const float p0 =
+                c <= lim && m_new != -INFINITY ? ex2(fmaf(x[c], p.scale_log2, -m_new)) : 0.f;
+            const float p1 = c + 1 <= lim && m_new != -INFINITY
+                                 ? ex2(fmaf(x[c + 1], p.scale_log2, -m_new))
+                                 : 0.f;
+            pk[c / 2] = pack16<BF16>(p0, p1);
+            psum += p0 + p1;
+          }
+        }
+        l = l * alpha + psum;
+        m = m_new;
+
+        if (jx >= 1) {  // PV of the previous tile done: O is stable and the P buffer free
+          ok = mbar_wait_bounded(smem_addr(o_done), (jx - 1) & 1);
+          if (__any_sync(0xffffffffu, !ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        if (j == it.ntiles - 1 && key0 + kPfKeys > it.L) {
+          // value rows past the cache's last position (stale slots, or not loaded) become zero,
+          // so that zero weights cannot meet a NaN; the tile's V copies must have landed first
+          ok = mbar_wait_bounded(smem_addr(v_full + (jx % kPfStages)), (jx / kPfStages) & 1);
+          if (__any_sync(0xffffffffu, !ok)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vst = sKV + 2 * (jx % kPfStages) * kKVBytes + kKVBytes;
+          const int r0 = it.L - key0;
+          const int nbytes16 = (kPfKeys - r0) * 8 * kRegions;  // 16-byte chunks to clear
+          for (int i = r; i < nbytes16; i += 128) {
+            const int c = i % (8 * kRegions), row = r0 + i / (8 * kRegions);
+            *reinterpret_cast<uint4*>(bp + (vst - base) + (c / 8) * kKVRegion + row * 128 +
+                                      (c % 8) * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        // P row r, swizzled K-major: 16-byte chunk c holds keys 8c .. 8c + 7
+        uint8_t* prow = bp + (sP - base);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(prow + sw128_offset(r, c)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-        for (int c = 0; c < D; c += 16) {
-          float v[16];
-          tmem_ld16(tO + lane_base + c, v);
+          for (int c = 0; c < D; c += 16) {
+            float v[16];
+            tmem_ld16(tO + lane_base + c, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] *= alpha;
-          tmem_st16(tO + lane_base + c, v);
+            for (int i = 0; i < 16; ++i) v[i] *= alpha;
+            tmem_st16(tO + lane_base + c, v);
+          }
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(p_full));
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(p_full));
-    }
-    if (ok) ok = mbar_wait_bounded(smem_addr(o_done), (ntiles - 1) & 1);
-    if (__any_sync(0xffffffffu, !ok)) {
-      if (lane == 0) {
-        flag_error(p.err, kErrTimeout);
-        *abort_flag = 1;
+      if (!ok) break;
+      // ---- epilogue of the item: O / l, then O is released to the next item's first PV
+      ok = mbar_wait_bounded(smem_addr(o_done), (jx - 1) & 1);
+      if (__any_sync(0xffffffffu, !ok)) {
+        ok = false;
+        break;
       }
-    } else {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                            (static_cast<size_t>(q0 + tr) * Hq + g * G + r % G) * D);
+      uint4* dst = reinterpret_cast<uint4*>(
+          static_cast<uint16_t*>(p.out) + (static_cast<size_t>(it.q0 + tr) * Hq + it.g * G + r % G) * D);
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t v[32];
@@ -468,7 +578,14 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             dst[c / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(o_free));
+        mbar_arrive(smem_addr(item_empty + slot));
+      }
     }
+    if (!ok && lane == 0) fail();
   }
 
   // ---- teardown: tensor memory is released once every warp is done with it
@@ -490,8 +607,8 @@ std::set<std::pair<const void*, int>>& pf_opted() {
 }
 
 template <int D, int G, bool BF16>
-cudaError_t launch_prefill(const CUtensorMap& km, const CUtensorMap& vm, const PrefillParams& p,
-                           dim3 grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                           const PrefillParams& p, unsigned grid, size_t smem, cudaStream_t stream) {
   auto fn = pa_prefill_kernel<D, G, BF16>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -506,19 +623,20 @@ cudaError_t launch_prefill(const CUtensorMap& km, const CUtensorMap& vm, const P
       pf_opted().insert(key);
     }
   }
-  fn<<<grid, kPfThreads, smem, stream>>>(km, vm, p);
+  fn<<<grid, kPfThreads, smem, stream>>>(qm, km, vm, p);
   return cudaGetLastError();
 }
 
 template <int D, bool BF16>
-cudaError_t launch_prefill_g(int group, const CUtensorMap& km, const CUtensorMap& vm,
-                             const PrefillParams& p, dim3 grid, size_t smem, cudaStream_t stream) {
+cudaError_t launch_prefill_g(int group, const CUtensorMap& qm, const CUtensorMap& km,
+                             const CUtensorMap& vm, const PrefillParams& p, unsigned grid,
+                             size_t smem, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_prefill<D, 1, BF16>(km, vm, p, grid, smem, stream);
-    case 2: return launch_prefill<D, 2, BF16>(km, vm, p, grid, smem, stream);
-    case 4: return launch_prefill<D, 4, BF16>(km, vm, p, grid, smem, stream);
-    case 8: return launch_prefill<D, 8, BF16>(km, vm, p, grid, smem, stream);
-    default: return launch_prefill<D, 16, BF16>(km, vm, p, grid, smem, stream);
+    case 1: return launch_prefill<D, 1, BF16>(qm, km, vm, p, grid, smem, stream);
+    case 2: return launch_prefill<D, 2, BF16>(qm, km, vm, p, grid, smem, stream);
+    case 4: return launch_prefill<D, 4, BF16>(qm, km, vm, p, grid, smem, stream);
+    case 8: return launch_prefill<D, 8, BF16>(qm, km, vm, p, grid, smem, stream);
+    default: return launch_prefill<D, 16, BF16>(qm, km, vm, p, grid, smem, stream);
   }
 }
 
@@ -570,17 +688,31 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
     msg = "q, out and the pools must be 16-byte aligned";
     return PA_EINVAL;
   }
+  const int tokens_per_tile = kPfRows / group;
+  const long long tiles = (a.max_q_len + tokens_per_tile - 1) / tokens_per_tile;
+  const long long total = static_cast<long long>(a.num_seqs) * a.num_kv_heads * tiles;
+  if (total >= (1ll << 30)) {
+    msg = "more than 2^30 work items (sequences x kv heads x query tiles)";
+    return PA_EUNSUPPORTED;
+  }
   const int urows = std::min(a.block_size, kPfKeys);
-  CUtensorMap kmap, vmap;
-  pa_status st = encode_pool_rows_map(&kmap, a.k_pool, rows, a.head_dim, 2, urows, msg);
+  CUtensorMap qmap, kmap, vmap;
+  pa_status st = encode_query_tile_map(&qmap, a.q, a.num_tokens, a.num_q_heads, a.head_dim, group,
+                                       tokens_per_tile, msg);
+  if (st != PA_OK) return st;
+  st = encode_pool_rows_map(&kmap, a.k_pool, rows, a.head_dim, 2, urows, msg);
   if (st != PA_OK) return st;
   st = encode_pool_rows_map(&vmap, a.v_pool, rows, a.head_dim, 2, urows, msg);
   if (st != PA_OK) return st;
 
   PrefillParams p{};
-  p.q = static_cast<const uint16_t*>(a.q);
   p.out = a.out;
+  p.block_tables = a.block_tables;
+  p.ctx_lens = a.ctx_lens;
+  p.q_starts = a.q_starts;
   p.err = a.err_flag;
+  p.work = a.work_counter;
+  p.num_tokens = a.num_tokens;
   p.num_q_heads = a.num_q_heads;
   p.num_kv_heads = a.num_kv_heads;
   p.block_size = a.block_size;
@@ -590,6 +722,8 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   while ((1 << p.log2_urows) < urows) ++p.log2_urows;
   p.num_blocks = a.num_blocks;
   p.max_blocks = a.max_blocks_per_seq;
+  p.tiles = static_cast<int>(tiles);
+  p.total = static_cast<int>(total);
   p.scale_log2 = a.scale * 1.4426950408889634f;
 
   const int D = a.head_dim;
@@ -597,28 +731,27 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   // no alignment slack: the kernel needs (and checks) a 1024-byte aligned dynamic region, and
   // two CTAs then fit on an SM
   const size_t smem = regions * kPfRows * 128 + kPfStages * 2 * regions * kPfKeys * 128 +
-                      kPfRows * 128 + 256;
-  const int tokens_per_tile = kPfRows / group;
-  const unsigned tiles = static_cast<unsigned>((a.max_q_len + tokens_per_tile - 1) / tokens_per_tile);
-  const bool bf16 = a.dtype == PA_BF16;
-  constexpr int kMaxZ = 65535;
-  for (int s0 = 0; s0 < a.num_seqs; s0 += kMaxZ) {
-    const int ns = std::min(kMaxZ, a.num_seqs - s0);
-    p.block_tables = a.block_tables + static_cast<size_t>(s0) * a.max_blocks_per_seq;
-    p.ctx_lens = a.ctx_lens + s0;
-    p.q_starts = a.q_starts + s0;
-    const dim3 grid(tiles, static_cast<unsigned>(a.num_kv_heads), static_cast<unsigned>(ns));
-    cudaError_t e;
-    if (D == 128)
-      e = bf16 ? launch_prefill_g<128, true>(group, kmap, vmap, p, grid, smem, stream)
-               : launch_prefill_g<128, false>(group, kmap, vmap, p, grid, smem, stream);
-    else
-      e = bf16 ? launch_prefill_g<64, true>(group, kmap, vmap, p, grid, smem, stream)
-               : launch_prefill_g<64, false>(group, kmap, vmap, p, grid, smem, stream);
-    st = cuda_status(e, "pa_prefill kernel launch", msg);
+                      kPfRows * 128 + kCtlBytes;
+  const int sms = device_sm_count();
+  if (sms <= 0) {
+    msg = "cannot read the SM count of the current device";
+    return PA_ECUDA;
+  }
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(2ll * sms, total));
+  if (a.work_counter != nullptr) {
+    st = cuda_status(cudaMemsetAsync(a.work_counter, 0, sizeof(int32_t), stream),
+                     "pa_prefill work counter reset", msg);
     if (st != PA_OK) return st;
   }
-  return PA_OK;
+  const bool bf16 = a.dtype == PA_BF16;
+  cudaError_t e;
+  if (D == 128)
+    e = bf16 ? launch_prefill_g<128, true>(group, qmap, kmap, vmap, p, grid, smem, stream)
+             : launch_prefill_g<128, false>(group, qmap, kmap, vmap, p, grid, smem, stream);
+  else
+    e = bf16 ? launch_prefill_g<64, true>(group, qmap, kmap, vmap, p, grid, smem, stream)
+             : launch_prefill_g<64, false>(group, qmap, kmap, vmap, p, grid, smem, stream);
+  return cuda_status(e, "pa_prefill kernel launch", msg);
 }
 
 }  // namespace pa

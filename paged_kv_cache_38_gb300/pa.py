@@ -199,6 +199,7 @@ class pa_prefill_args(ctypes.Structure):
         ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
         ("max_blocks_per_seq", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
         ("dtype", ctypes.c_int), ("scale", ctypes.c_float), ("err_flag", ctypes.c_void_p),
+        ("work_counter", ctypes.c_void_p),
     ]
 
 
@@ -206,9 +207,13 @@ def pa_prefill(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                block_tables: torch.Tensor, ctx_lens: torch.Tensor, q_starts: torch.Tensor,
                scale: float, *, out: Optional[torch.Tensor] = None,
                max_q_len: Optional[int] = None, err_flag: Optional[torch.Tensor] = None,
+               work_counter: Optional[torch.Tensor] = None, dynamic: bool = True,
                stream=None) -> torch.Tensor:
     """Causal attention of each sequence's chunk of query tokens (rows q_starts[s] ..
-    q_starts[s + 1] - 1 of q [num_tokens][num_q_heads][head_dim]) over its paged cache."""
+    q_starts[s + 1] - 1 of q [num_tokens][num_q_heads][head_dim]) over its paged cache.
+
+    dynamic: the persistent CTAs take work items from an int32 counter (work_counter, or one
+    allocated for the call); False assigns them round-robin."""
     if out is None:
         out = torch.empty_like(q)
     dt = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}.get(q.dtype)
@@ -226,6 +231,11 @@ def pa_prefill(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
     a.max_blocks_per_seq = block_tables.shape[1] if block_tables.dim() == 2 else 0
     a.max_q_len, a.dtype, a.scale = int(max_q_len), dt, float(scale)
     a.err_flag = _ptr(err_flag)
+    if dynamic and work_counter is None:
+        work_counter = torch.empty(1, dtype=torch.int32, device=q.device)
+        if stream is not None and hasattr(stream, "cuda_stream"):
+            work_counter.record_stream(stream)
+    a.work_counter = _ptr(work_counter) if dynamic else None
     _check(lib().pa_prefill(ctypes.byref(a), _stream(stream)))
     return out
 

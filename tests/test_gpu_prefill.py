@@ -145,3 +145,26 @@ def test_prefill_chunk_longer_than_max_q_len_flagged():
     assert torch.count_nonzero(out[:covered]).item() == 0
     ref = _oracle(case, qs.cpu(), q.cpu())
     assert _err(out[300:], ref[300:]) <= TOL["bf16"]  # the other sequence is unaffected
+
+
+def test_prefill_work_distribution():
+    """More work items (query tiles x kv heads x sequences) than the persistent CTAs: the
+    dynamic work counter and the round-robin assignment give the same bits, both matching the
+    oracle; an explicit counter left dirty by a previous call is reset by the call itself."""
+    spec = synth.DecodeSpec("pf_many", 40, 32, 8, 128, 16, "bf16", "bf16", ctx_range=(1, 700))
+    case = synth.make_case(spec, seed=77)
+    qs, q = synth.prefill_queries(case, seed=8)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    qd, qsd = q.cuda(), qs.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for kw in (dict(dynamic=False),
+               dict(work_counter=torch.full((1,), 12345, dtype=torch.int32, device="cuda")),
+               dict()):
+        outs.append(pa.pa_prefill(qd, g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qsd,
+                                  case.scale, err_flag=err, **kw))
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _err(outs[0], ref) <= TOL["bf16"]
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
