@@ -71,7 +71,8 @@ typedef enum {
 /* Bits OR-ed into the optional device error flag. */
 #define PA_ERR_BLOCK_ID 1 /* block table entry, slot or pair outside [0, num_blocks) */
 #define PA_ERR_CTX_LEN 2  /* ctx_len < 0, > max_ctx_len or > max_blocks_per_seq*block_size;
-                              prefill: a chunk longer than its ctx_len or than max_q_len */
+                              prefill: a chunk longer than its ctx_len or than max_q_len
+                              (rounded up to whole query tiles) */
 #define PA_ERR_TIMEOUT 4  /* a bounded wait inside a kernel expired */
 
 /*
@@ -153,9 +154,10 @@ pa_status pa_decode(const pa_decode_args* args, pa_stream stream);
  * computed on the tensor cores (tcgen05.mma, fp32 accumulation in tensor memory).
  *   q, out        device [num_tokens][num_q_heads][head_dim], dtype, 16-byte aligned
  *   q_starts      device int32 [num_seqs + 1], non-decreasing, q_starts[num_seqs] = num_tokens
- *   max_q_len     host upper bound of the chunk lengths (sizes the grid)
- * A sequence with n > L, L > max_blocks_per_seq * block_size or n > max_q_len sets
- * PA_ERR_CTX_LEN and its rows are zero (with n > max_q_len, those past max_q_len are not
+ *   max_q_len     host upper bound of the chunk lengths (sizes the work: query tiles of
+ *                 128 / G tokens per (sequence, kv head))
+ * A sequence with n > L, L > max_blocks_per_seq * block_size or n above max_q_len rounded up to
+ * whole query tiles sets PA_ERR_CTX_LEN and its rows are zero (past that bound they are not
  * written); an out-of-pool block id sets PA_ERR_BLOCK_ID (those rows are then unspecified).
  * Supported: dtype PA_F16 or PA_BF16 (q, K/V and out alike); head_dim 64 or 128; block_size 8,
  * 16, 32 or 64; group size 1, 2, 4, 8 or 16.
