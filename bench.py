@@ -483,26 +483,30 @@ def prefill_flops(ctx_lens, q_starts, num_q_heads: int, head_dim: int) -> int:
 def run_prefill_bench(dev, flush, peaks) -> dict:
     """pa_prefill on the GQA geometry (32 q / 8 kv heads x 128, bf16, 16-token blocks):
     16 whole 2,048-token prompts, and 64 chunks of 512 new tokens on 1,536-token histories
-    (chunked prefill / recompute). Causal flops per second against the measured bf16 GEMM
-    peak."""
+    (chunked prefill / recompute); then other head geometries on 8 whole 2,048-token prompts:
+    MHA (32 / 32 x 128, f16), a group of 8 (64 / 8 x 128) and head_dim 64 (32 / 8 x 64).
+    Causal flops per second against the measured bf16 GEMM peak."""
     import paged_kv_cache_38_gb300 as pa
 
     out = {}
-    for name, lens, chunk in (("prompts_16x2048", [2048] * 16, 2048),
-                              ("chunks_64x512_on_2048", [2048] * 64, 512)):
-        spec = synth.DecodeSpec(name, len(lens), 32, 8, 128, 16, "bf16", "bf16",
-                                ctx_lens=tuple(lens))
+    for name, lens, chunk, hq, hkv, d, dt in (
+            ("prompts_16x2048", [2048] * 16, 2048, 32, 8, 128, "bf16"),
+            ("chunks_64x512_on_2048", [2048] * 64, 512, 32, 8, 128, "bf16"),
+            ("mha_prompts_8x2048", [2048] * 8, 2048, 32, 32, 128, "f16"),
+            ("g8_prompts_8x2048", [2048] * 8, 2048, 64, 8, 128, "bf16"),
+            ("d64_prompts_8x2048", [2048] * 8, 2048, 32, 8, 64, "bf16")):
+        spec = synth.DecodeSpec(name, len(lens), hq, hkv, d, 16, dt, dt, ctx_lens=tuple(lens))
         case = synth.make_case(spec, seed=SEED, device=dev, logical=False, poison=False)
         n = [chunk] * len(lens)
         qs = torch.tensor(np.concatenate([[0], np.cumsum(n)]), dtype=torch.int32, device=dev)
-        q = torch.randn(int(qs[-1]), 32, 128, device=dev).to(torch.bfloat16)
+        q = torch.randn(int(qs[-1]), hq, d, device=dev).to(synth.TORCH_DTYPES[dt])
         o = torch.empty_like(q)
         call = lambda: pa.pa_prefill(q, case.k_pool, case.v_pool, case.block_tables,  # noqa: E731
                                      case.ctx_lens, qs, case.scale, out=o, max_q_len=chunk)
         for _ in range(3):
             call()
         t = statistics.mean(time_steps(call, 10, flush))
-        fl = prefill_flops(lens, qs.cpu().numpy(), 32, 128)
+        fl = prefill_flops(lens, qs.cpu().numpy(), hq, d)
         tf = fl / (t * 1e-3) / 1e12
         out[name] = {"ms": round(t, 4), "tflops": round(tf, 1),
                      "pct_of_bf16_peak": round(100 * tf / peaks["bf16_tflops"], 1),
