@@ -168,3 +168,37 @@ def test_prefill_work_distribution():
     assert int(err.item()) == 0
     assert _err(outs[0], ref) <= TOL["bf16"]
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+def test_prefill_in_cuda_graph_bitwise():
+    """pa_prefill captured in a CUDA graph (the work counter's reset and the persistent kernel
+    both in the graph) and replayed gives the eager call's bits, replay after replay."""
+    spec = synth.DecodeSpec("pf_graph", 6, 32, 8, 128, 16, "bf16", "bf16", ctx_range=(50, 900))
+    case = synth.make_case(spec, seed=31)
+    qs, q = synth.prefill_queries(case, seed=12)
+    g = case.to("cuda")
+    qd, qsd = q.cuda(), qs.cuda()
+    max_q = int((qs[1:] - qs[:-1]).max())
+    counter = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(qd)
+
+    def call():
+        pa.pa_prefill(qd, g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qsd, case.scale,
+                      out=out, max_q_len=max_q, work_counter=counter)
+
+    call()
+    torch.cuda.synchronize()
+    eager = out.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(2):
+        out.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
