@@ -162,9 +162,9 @@ pa_status pa_decode(const pa_decode_args* args, pa_stream stream);
  * Supported: dtype PA_F16 or PA_BF16 (q, K/V and out alike); head_dim 64 or 128; block_size 8,
  * 16, 32 or 64; group size 1, 2, 4, 8 or 16.
  * The kernel is persistent (two CTAs per SM). With work_counter set, the call zeroes that int32
- * on the stream and the CTAs take work items from it, longest first within each (sequence, kv
- * head); NULL assigns the items round-robin. The counter must not be shared by calls that can
- * run at the same time.
+ * on the stream and the CTAs take work items from it: the 4 longest query tiles of every
+ * (sequence, kv head), then the next 4, and so on; NULL assigns the same items round-robin.
+ * The counter must not be shared by calls that can run at the same time.
  */
 typedef struct {
   const void* q;

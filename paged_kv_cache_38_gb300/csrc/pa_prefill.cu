@@ -10,8 +10,10 @@
 // tensor-memory columns each at head_dim 128, so the two overlap each other's softmax and MMA
 // phases). A work item is one tile of 128 query rows of one (sequence, kv head); a row is one
 // (token, query head of the group), so a tile holds 128 / G tokens and the GQA group shares
-// every K/V tile. Items are taken longest first within each (sequence, kv head), from a work
-// counter or round-robin; tensor memory, barriers and the K/V rings live across items, so the
+// every K/V tile. Items are taken from a work counter (or round-robin) in blocks of kTileBlock
+// query tiles: the kTileBlock longest tiles of every (sequence, kv head), then the next
+// kTileBlock, and so on, so that the batch runs roughly longest first while the pairs in flight
+// keep their K/V in L2. Tensor memory, barriers and the K/V rings live across items, so the
 // next item's queries and first K/V tiles load while the current one finishes. Roles:
 //   * warp 3 takes items and publishes them through a 2-slot ring; it loads each item's query
 //     tile (one 3-D TMA box per 64 columns) once the previous item's last S MMA has completed;
@@ -48,6 +50,7 @@ constexpr int kPfRows = 128;      // query rows per tile = MMA M
 constexpr int kPfKeys = 64;       // keys per K/V tile: S columns, PV reduction
 constexpr int kPfStages = 2;      // K/V ring depth (two CTAs fit on an SM)
 constexpr int kSlots = 2;         // published work items
+constexpr int kTileBlock = 4;     // query tiles of one (sequence, kv head) per block of the order
 constexpr int kSoftmaxWarp0 = 4;  // warps 4..7 form the softmax warpgroup
 constexpr int kItemReaders = 3 + 4;  // K producer, V producer, MMA issuer, 4 softmax warps
 constexpr uint32_t kTmemCols = 256;  // O at columns [0, head_dim), S buffers at [128, 192), [192, 256)
@@ -63,7 +66,9 @@ struct PrefillParams {
   int num_tokens, num_q_heads, num_kv_heads, block_size, log2_block, num_blocks, max_blocks;
   int log2_urows;    // rows per K/V copy: min(block_size, 64)
   int tiles;         // query tiles per (sequence, kv head) at the longest chunk (max_q_len)
-  int total;         // num_seqs * num_kv_heads * tiles
+  int tile_block;    // min(kTileBlock, tiles)
+  int pairs;         // num_seqs * num_kv_heads
+  int total;         // pairs * tiles rounded up to whole blocks
   float scale_log2;  // scale * log2(e)
 };
 
@@ -179,8 +184,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
                             : static_cast<int>(blockIdx.x) + fetched * static_cast<int>(gridDim.x);
           ++fetched;
           if (v >= p.total) break;
-          const int sg = v / p.tiles;
-          const int tile = p.tiles - 1 - (v - sg * p.tiles);  // longest tile of (s, g) first
+          const int per_block = p.pairs * p.tile_block;
+          const int blk = v / per_block, rem = v - blk * per_block;
+          const int sg = rem / p.tile_block;
+          const int tile = p.tiles - 1 - (blk * p.tile_block + (rem - sg * p.tile_block));
+          if (tile < 0) continue;  // past the shortest tile (the last block is partial)
           const int s = sg / p.num_kv_heads, g = sg - s * p.num_kv_heads;
           const int q0 = __ldg(p.q_starts + s);
           const int n = __ldg(p.q_starts + s + 1) - q0;
@@ -690,7 +698,9 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   }
   const int tokens_per_tile = kPfRows / group;
   const long long tiles = (a.max_q_len + tokens_per_tile - 1) / tokens_per_tile;
-  const long long total = static_cast<long long>(a.num_seqs) * a.num_kv_heads * tiles;
+  const long long tile_block = std::min<long long>(kTileBlock, tiles);
+  const long long total = (tiles + tile_block - 1) / tile_block * tile_block *
+                          static_cast<long long>(a.num_seqs) * a.num_kv_heads;
   if (total >= (1ll << 30)) {
     msg = "more than 2^30 work items (sequences x kv heads x query tiles)";
     return PA_EUNSUPPORTED;
@@ -723,6 +733,8 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   p.num_blocks = a.num_blocks;
   p.max_blocks = a.max_blocks_per_seq;
   p.tiles = static_cast<int>(tiles);
+  p.tile_block = static_cast<int>(tile_block);
+  p.pairs = a.num_seqs * a.num_kv_heads;
   p.total = static_cast<int>(total);
   p.scale_log2 = a.scale * 1.4426950408889634f;
 
