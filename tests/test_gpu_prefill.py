@@ -202,3 +202,24 @@ def test_prefill_in_cuda_graph_bitwise():
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, eager)
+
+
+def test_prefill_out_of_pool_block_flagged():
+    """A block-table entry outside the pool sets PA_ERR_BLOCK_ID; the other sequences of the
+    launch are unaffected (their rows still match the oracle)."""
+    spec = synth.DecodeSpec("pf_badblk", 4, 16, 4, 128, 16, "bf16", "bf16", ctx_lens=(200, 120, 300, 90))
+    case = synth.make_case(spec, seed=21)
+    qs, q = synth.prefill_queries(case, seed=3, whole=True)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    bt = g.block_tables.clone()
+    bt[1, 2] = g.k_pool.shape[0] + 5  # sequence 1 reads a block past the pool
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, bt, g.ctx_lens, qs.cuda(), case.scale,
+                        err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_ERR_BLOCK_ID
+    lo, hi = int(qs[1]), int(qs[2])
+    keep = torch.cat([out[:lo], out[hi:]])
+    want = np.concatenate([ref[:lo], ref[hi:]])
+    assert _err(keep, want) <= TOL["bf16"]
