@@ -321,6 +321,15 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_f16(kPfRows, kPfKeys, BF16, false);
+      // Shared-memory descriptors are built once: an operand at byte offset o from a base has
+      // the base's descriptor plus o / 16 in the start-address field (no carry: every address
+      // is below 256 KB). The tensor pipe cannot run ahead of this thread, so every instruction
+      // between two MMAs lengthens the MMA stream; with the descriptors rebuilt per MMA the
+      // attention sequence ran at half the pipe's rate.
+      const uint64_t dQ = umma_sdesc(sQ, 16, 1024);
+      const uint64_t dK = umma_sdesc(sKV, 16, 1024);
+      const uint64_t dP = umma_sdesc(sP, 16, 1024);
+      const uint64_t dV = umma_sdesc(sKV + kKVBytes, kKVRegion, 1024);
       constexpr uint32_t idO = umma_idesc_f16(kPfRows, D, BF16, true);
       // Two cursors over the items: S_ns is issued as soon as K_ns has landed (and its S buffer
       // is free, and at an item's first tile its queries have landed), PV_npv as soon as P_npv
@@ -359,12 +368,13 @@ __global__ void __launch_bounds__(kPfThreads, 2)
               (ns < 2 || mbar_test(smem_addr(s_free + b), ((ns >> 1) - 1) & 1)) &&
               (jS > 0 || mbar_test(smem_addr(q_full), kS & 1))) {
             tc_fence_after();
-            const uint32_t kst = sKV + 2 * st * kKVBytes;
+            const uint64_t dKs = dK + ((2u * st * kKVBytes) >> 4);
+            const uint32_t dS = tS + 64 * b;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
+              constexpr uint32_t kQStep = kQRegion >> 4, kKStep = kKVRegion >> 4;
               const uint32_t c = k / 4, kk = k % 4;
-              umma_f16(tS + 64 * b, umma_sdesc(sQ + c * kQRegion + kk * 32, 16, 1024),
-                       umma_sdesc(kst + c * kKVRegion + kk * 32, 16, 1024), idS, k > 0);
+              umma_f16(dS, dQ + (c * kQStep + kk * 2), dKs + (c * kKStep + kk * 2), idS, k > 0);
             }
             umma_commit(smem_addr(s_full + b));
             umma_commit(smem_addr(k_empty + st));
@@ -393,11 +403,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
               mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1) &&
               (jP > 0 || nO == 0 || mbar_test(smem_addr(o_free), (nO - 1) & 1))) {
             tc_fence_after();
-            const uint32_t vst = sKV + 2 * stp * kKVBytes + kKVBytes;
+            const uint64_t dVs = dV + ((2u * stp * kKVBytes) >> 4);
 #pragma unroll
             for (int k = 0; k < kPfKeys / 16; ++k)
-              umma_f16(tO, umma_sdesc(sP + k * 32, 16, 1024),
-                       umma_sdesc(vst + k * 16 * 128, kKVRegion, 1024), idO, jP > 0 || k > 0);
+              umma_f16(tO, dP + k * 2, dVs + k * 128, idO, jP > 0 || k > 0);
             umma_commit(smem_addr(o_done));
             umma_commit(smem_addr(v_empty + stp));
             ++npv;
