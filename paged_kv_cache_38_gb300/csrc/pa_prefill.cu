@@ -22,7 +22,8 @@
 //     2-stage ring;
 //   * warp 1 allocates tensor memory and one lane issues the MMAs: S_j = Q K_j^T (M 128, N 64)
 //     into one of two TMEM S buffers, and O += P_j V_j (M 128, N = head_dim) into the TMEM O
-//     accumulator, each completion signalled by tcgen05.commit on an mbarrier;
+//     accumulator; one tcgen05.commit per MMA group signals its completion on an mbarrier,
+//     which also hands the group's K (or V) stage back to its producer;
 //   * warps 4-7 (one thread per row) read S with tcgen05.ld, apply the causal mask and the
 //     online softmax (log2 domain), write P (16-bit, swizzled K-major) to shared memory and
 //     rescale O in tensor memory when a row's running maximum grows; at the end of an item they
@@ -116,16 +117,21 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   uint8_t* ctl = bp + (sP - base) + kPfRows * 128;
   // K and V stream through separate rings: K of tile j is free once S_j is computed, V once
   // PV_j is, so K loads run a whole softmax ahead of V loads. Every phase below counts tiles
-  // (or items) over the whole run of the CTA.
+  // (or items) over the whole run of the CTA. Tile j uses stage j % 2 of both rings, S buffer
+  // j % 2 and completion barriers s_full[j % 2] and o_done[j % 2]; with one commit per MMA
+  // group (a second one per group slows the MMA stream by about a tenth), those two barriers
+  // also release the stage's K and V to the producers (each producer waits on every phase of
+  // its own stage, so a parity wait cannot pass on a phase that is still one behind). The query
+  // loader does not see every phase of s_full, so the query buffer has its own barrier,
+  // committed after an item's last S.
+  static_assert(kPfStages == 2, "the completion barriers double as the rings' empty barriers");
   uint64_t* k_full = reinterpret_cast<uint64_t*>(ctl);  // [kPfStages]
-  uint64_t* k_empty = k_full + kPfStages;                // [kPfStages]
-  uint64_t* v_full = k_empty + kPfStages;                // [kPfStages]
-  uint64_t* v_empty = v_full + kPfStages;                // [kPfStages]
-  uint64_t* s_full = v_empty + kPfStages;                // [2]
+  uint64_t* v_full = k_full + kPfStages;                 // [kPfStages]
+  uint64_t* s_full = v_full + kPfStages;                 // [2] S_j complete: K_j free too
   uint64_t* s_free = s_full + 2;                         // [2]
   uint64_t* p_full = s_free + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* o_free = o_done + 1;                         // O read by the epilogue (4 warps)
+  uint64_t* o_done = p_full + 1;                         // [2] PV_j complete: V_j free too
+  uint64_t* o_free = o_done + 2;                         // O read by the epilogue (4 warps)
   uint64_t* q_full = o_free + 1;                         // the item's query tile landed
   uint64_t* q_empty = q_full + 1;                        // the item's last S complete
   uint64_t* item_full = q_empty + 1;                     // [kSlots]
@@ -139,16 +145,14 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     *abort_flag = 0;
     for (int i = 0; i < kPfStages; ++i) {
       mbar_init(smem_addr(k_full + i), 1);
-      mbar_init(smem_addr(k_empty + i), 1);
       mbar_init(smem_addr(v_full + i), 1);
-      mbar_init(smem_addr(v_empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(s_full + i), 1);
       mbar_init(smem_addr(s_free + i), 4);
+      mbar_init(smem_addr(o_done + i), 1);
     }
     mbar_init(smem_addr(p_full), 4);
-    mbar_init(smem_addr(o_done), 1);
     mbar_init(smem_addr(o_free), 4);
     mbar_init(smem_addr(q_full), 1);
     mbar_init(smem_addr(q_empty), 1);
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       const bool is_v = warp == 2;
       const CUtensorMap* map = is_v ? &vmap : &kmap;
       uint64_t* fullb = is_v ? v_full : k_full;
-      uint64_t* emptyb = is_v ? v_empty : k_empty;
+      uint64_t* emptyb = is_v ? o_done : s_full;  // stage st of tile J - 2 consumed
       const uint64_t pol = policy_evict_normal();  // the sequence's other query tiles reread them
       const int urows = 1 << p.log2_urows, B = p.block_size;
       const int units = kPfKeys >> p.log2_urows;
@@ -377,7 +381,6 @@ __global__ void __launch_bounds__(kPfThreads, 2)
               umma_f16(dS, dQ + (c * kQStep + kk * 2), dKs + (c * kKStep + kk * 2), idS, k > 0);
             }
             umma_commit(smem_addr(s_full + b));
-            umma_commit(smem_addr(k_empty + st));
             ++ns;
             if (++jS == iS.ntiles) {
               umma_commit(smem_addr(q_empty));
@@ -407,8 +410,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 #pragma unroll
             for (int k = 0; k < kPfKeys / 16; ++k)
               umma_f16(tO, dP + k * 2, dVs + k * 128, idO, jP > 0 || k > 0);
-            umma_commit(smem_addr(o_done));
-            umma_commit(smem_addr(v_empty + stp));
+            umma_commit(smem_addr(o_done + stp));
             ++npv;
             if (++jP == iP.ntiles) {
               ++nO;
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         m = m_new;
 
         if (jx >= 1) {  // PV of the previous tile done: O is stable and the P buffer free
-          ok = mbar_wait_bounded(smem_addr(o_done), (jx - 1) & 1);
+          ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1);
           if (__any_sync(0xffffffffu, !ok)) {
             ok = false;
             break;
@@ -571,7 +573,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       }
       if (!ok) break;
       // ---- epilogue of the item: O / l, then O is released to the next item's first PV
-      ok = mbar_wait_bounded(smem_addr(o_done), (jx - 1) & 1);
+      ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1);
       if (__any_sync(0xffffffffu, !ok)) {
         ok = false;
         break;
