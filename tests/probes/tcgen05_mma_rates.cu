@@ -16,6 +16,11 @@
 //   6  mode 5 with S_x double-buffered at columns c and c + 64 (one 128-column group), the
 //      buffer alternating tile by tile
 //   7  mode 6 with one commit after the S pair and one after the PV pair
+// Modes 0-7 build each MMA's descriptors in the issue loop; modes 8-10 build them before the
+// loop and unroll each group, so that only the MMAs (and commits) are issued:
+//   8  mode 6's sequence (S double-buffered, as in the prefill kernel)
+//   9  mode 4's sequence with one commit after each group
+//  10  mode 4's sequence with two commits after each group
 // Every wait is bounded; a timeout is reported as status 1.
 #include <cuda_runtime.h>
 
@@ -71,7 +76,7 @@ __device__ bool wait_bounded(uint32_t bar, uint32_t parity) {
   }
 }
 
-constexpr int kMmas = 672;  // a multiple of 12 and of 24 (whole groups in modes 4-7)
+constexpr int kMmas = 672;  // a multiple of 12 and of 24 (whole groups in modes 4-10)
 
 template <int MODE>
 __global__ void rates(long long* out, int* status) {
@@ -96,7 +101,48 @@ __global__ void rates(long long* out, int* status) {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t t = tbase;
   const uint32_t a = saddr(sm), b = a + 32768;  // A: 32 KB, B: 32 KB
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && MODE >= 8) {
+    uint64_t dq[4], dk[4], dp[4], dv[4];  // S: Q and K steps; PV: P and V steps
+    for (int k = 0; k < 4; ++k) {
+      dq[k] = desc(a + k * 32, 16, 1024);
+      dk[k] = desc(b + k * 32, 16, 1024);
+      dp[k] = desc(a + 16384 + k * 32, 16, 1024);
+      dv[k] = desc(b + k * 2048, 8192, 1024);
+    }
+    const uint32_t idS = idesc(128, 64, 0), idO = idesc(128, 128, 1);
+    const long long c0 = clock64();
+    if (MODE == 8) {
+      for (int tile = 0; tile < kMmas / 24; ++tile) {
+        const uint32_t sbuf = 64u * (tile & 1);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mma_ss(t + 256 + 128 * x + sbuf, dq[k & 3], dk[k & 3], idS);
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ss(t + 128 * x, dp[k], dv[k], idO);
+      }
+    } else {
+      for (int tile = 0; tile < kMmas / 12; ++tile) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mma_ss(t + 256, dq[k & 3], dk[k & 3], idS);
+        commit(saddr(&groups));
+        if (MODE == 10) commit(saddr(&groups));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mma_ss(t, dp[k], dv[k], idO);
+        commit(saddr(&groups));
+        if (MODE == 10) commit(saddr(&groups));
+      }
+    }
+    const long long c1 = clock64();
+    commit(saddr(&done));
+    const bool ok = wait_bounded(saddr(&done), 0);
+    const long long c2 = clock64();
+    out[0] = c1 - c0;
+    out[1] = c2 - c0;
+    if (!ok) *status = 1;
+  } else if (threadIdx.x == 0) {
     const long long c0 = clock64();
     for (int i = 0; i < kMmas; ++i) {
       const int k = i & 3;
@@ -155,15 +201,19 @@ int main() {
   long long* d = nullptr;
   int* st = nullptr;
   if (cudaMalloc(&d, 16) != cudaSuccess || cudaMalloc(&st, 4) != cudaSuccess) return 2;
-  const char* names[8] = {"N64 smem A", "N128 smem A", "N128 tmem A (PV)", "N256 smem A",
-                          "S / PV alternating, one query tile", "attention, S at fixed columns",
-                          "attention, S double-buffered in one 128-column group",
-                          "attention, S double-buffered, commits"};
+  constexpr int kModes = 11;
+  const char* names[kModes] = {"N64 smem A", "N128 smem A", "N128 tmem A (PV)", "N256 smem A",
+                               "S / PV alternating, one query tile", "attention, S at fixed columns",
+                               "attention, S double-buffered in one 128-column group",
+                               "attention, S double-buffered, commits",
+                               "attention, S double-buffered (mode 6), precomputed",
+                               "one query tile, precomputed, 1 commit per group",
+                               "one query tile, precomputed, 2 commits per group"};
   // flops per MMA averaged over the mode's sequence
   const double f64 = 128.0 * 64 * 16 * 2, f128 = 128.0 * 128 * 16 * 2;
   const double mix = (16 * f64 + 8 * f128) / 24;
-  const double flops[8] = {f64, f128, f128, 2 * f128, (8 * f64 + 4 * f128) / 12, mix, mix, mix};
-  for (int mode = 0; mode < 8; ++mode) {
+  const double flops[kModes] = {f64, f128, f128, 2 * f128, mix, mix, mix, mix, mix, mix, mix};
+  for (int mode = 0; mode < kModes; ++mode) {
     long long h[2] = {0, 0};
     int hs = 0;
     for (int rep = 0; rep < 3; ++rep) {  // the last of three runs is reported
@@ -177,7 +227,10 @@ int main() {
         case 4: e = launch<4>(d, st); break;
         case 5: e = launch<5>(d, st); break;
         case 6: e = launch<6>(d, st); break;
-        default: e = launch<7>(d, st); break;
+        case 7: e = launch<7>(d, st); break;
+        case 8: e = launch<8>(d, st); break;
+        case 9: e = launch<9>(d, st); break;
+        default: e = launch<10>(d, st); break;
       }
       if (e == cudaSuccess) e = cudaDeviceSynchronize();
       if (e != cudaSuccess) {
