@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       // Two cursors over the items: S_ns is issued as soon as K_ns has landed (and its S buffer
       // is free, and at an item's first tile its queries have landed), PV_npv as soon as P_npv
       // and V_npv are ready (and, at an item's first tile, once the epilogue has read O),
-      // whichever comes first. S runs ahead of PV by up to two tiles, across item boundaries.
+      // whichever comes first, PV before S when both are. S runs ahead of PV by up to two
+      // tiles, across item boundaries.
       int kS = 0, jS = 0, ns = 0;   // S stream: item, tile in item, S issued over all items
       bool haveS = false, endS = false;
       PfItem iS{};
@@ -355,6 +356,38 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           break;
         }
         bool did = false;
+        // ---- PV stream (first: PV_j stands between P_j and the softmax's write of P_{j+1},
+        // while S runs up to two tiles ahead)
+        if (!haveP) {
+          if (kP < kS || (kP == kS && haveS)) {
+            iP = items[kP % kSlots];
+            haveP = true;
+            jP = 0;
+          } else if (endS && kP == kS) {
+            break;  // every item is done
+          }
+        }
+        if (haveP && npv < ns) {
+          const int stp = npv % kPfStages;
+          if (mbar_test(smem_addr(p_full), npv & 1) &&
+              mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1) &&
+              (jP > 0 || nO == 0 || mbar_test(smem_addr(o_free), (nO - 1) & 1))) {
+            tc_fence_after();
+            const uint64_t dVs = dV + ((2u * stp * kKVBytes) >> 4);
+#pragma unroll
+            for (int k = 0; k < kPfKeys / 16; ++k)
+              umma_f16(tO, dP + k * 2, dVs + k * 128, idO, jP > 0 || k > 0);
+            umma_commit(smem_addr(o_done + stp));
+            ++npv;
+            if (++jP == iP.ntiles) {
+              ++nO;
+              mbar_arrive(smem_addr(item_empty + kP % kSlots));
+              haveP = false;
+              ++kP;
+            }
+            did = true;
+          }
+        }
         // ---- S stream
         if (!haveS && !endS && mbar_test(smem_addr(item_full + kS % kSlots), (kS / kSlots) & 1)) {
           iS = items[kS % kSlots];
@@ -386,37 +419,6 @@ __global__ void __launch_bounds__(kPfThreads, 2)
               umma_commit(smem_addr(q_empty));
               haveS = false;
               ++kS;
-            }
-            did = true;
-          }
-        }
-        // ---- PV stream
-        if (!haveP) {
-          if (kP < kS || (kP == kS && haveS)) {
-            iP = items[kP % kSlots];
-            haveP = true;
-            jP = 0;
-          } else if (endS && kP == kS) {
-            break;  // every item is done
-          }
-        }
-        if (haveP && npv < ns) {
-          const int stp = npv % kPfStages;
-          if (mbar_test(smem_addr(p_full), npv & 1) &&
-              mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1) &&
-              (jP > 0 || nO == 0 || mbar_test(smem_addr(o_free), (nO - 1) & 1))) {
-            tc_fence_after();
-            const uint64_t dVs = dV + ((2u * stp * kKVBytes) >> 4);
-#pragma unroll
-            for (int k = 0; k < kPfKeys / 16; ++k)
-              umma_f16(tO, dP + k * 2, dVs + k * 128, idO, jP > 0 || k > 0);
-            umma_commit(smem_addr(o_done + stp));
-            ++npv;
-            if (++jP == iP.ntiles) {
-              ++nO;
-              mbar_arrive(smem_addr(item_empty + kP % kSlots));
-              haveP = false;
-              ++kP;
             }
             did = true;
           }
