@@ -57,6 +57,36 @@ constexpr int kItemReaders = 3 + 4;  // K producer, V producer, MMA issuer, 4 so
 constexpr uint32_t kTmemCols = 256;  // O at columns [0, head_dim), S buffers at [128, 192), [192, 256)
 constexpr uint32_t kCtlBytes = 384;  // barriers, item slots, tensor-memory address, abort flag
 
+// Softmax arithmetic on full tiles: 3-input maxima and packed fp32 pairs (fma / add .f32x2)
+// halve the instruction count of the row maximum, the exponent arguments and the row sum; the
+// softmax warps share their schedulers with the other CTA's and are bound by issue.
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// two fp32 lanes in one 64-bit register pair
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// (a * b + c) per lane, rounded once (the same result as two fmaf)
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 struct PrefillParams {
   void* out;
   const int32_t* block_tables;
@@ -488,8 +518,17 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const int lim = row_valid ? pos - key0 : -1;  // last visible column (full: >= 63)
         float mt = -INFINITY;
         if (full) {
+          // four independent chains of 3-input maxima over 16 scores each
+          float a[4];
 #pragma unroll
-          for (int c = 0; c < kPfKeys; ++c) mt = fmaxf(mt, x[c]);
+          for (int q = 0; q < 4; ++q) {
+            const float* y = x + 16 * q;
+            float t = fmax3(y[0], y[1], y[2]);
+#pragma unroll
+            for (int i = 3; i < 15; i += 2) t = fmax3(t, y[i], y[i + 1]);
+            a[q] = fmaxf(t, y[15]);
+          }
+          mt = fmax3(a[0], a[1], fmaxf(a[2], a[3]));
         } else {
 #pragma unroll
           for (int c = 0; c < kPfKeys; ++c)
@@ -505,13 +544,20 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         uint32_t pk[kPfKeys / 2];
         float psum = 0.f;
         if (full) {
+          // pairs of scores through one packed FMA; the row sum in two packed partial sums
+          const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_new, -m_new);
+          uint64_t s2 = f2pack(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < kPfKeys; c += 2) {
-            const float p0 = ex2(fmaf(x[c], p.scale_log2, -m_new));
-            const float p1 = ex2(fmaf(x[c + 1], p.scale_log2, -m_new));
+            float t0, t1;
+            f2unpack(ffma2(f2pack(x[c], x[c + 1]), sc2, nm2), t0, t1);
+            const float p0 = ex2(t0), p1 = ex2(t1);
             pk[c / 2] = pack16<BF16>(p0, p1);
-            psum += p0 + p1;
+            s2 = fadd2(s2, f2pack(p0, p1));
           }
+          float s0, s1;
+          f2unpack(s2, s0, s1);
+          psum = s0 + s1;
         } else {
 #pragma unroll
           for (int c = 0; c < kPfKeys; c += 2) {
