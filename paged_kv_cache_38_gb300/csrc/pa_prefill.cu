@@ -630,19 +630,26 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(
           static_cast<uint16_t*>(p.out) + (static_cast<size_t>(it.q0 + tr) * Hq + it.g * G + r % G) * D);
+      // two 32-column loads per wait: the epilogue stands between an item's last PV and the
+      // next item's first tile, so each tensor-memory round trip shows
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32_nowait(tO + lane_base + c, v);
+      for (int c = 0; c < D; c += 64) {
+        uint32_t v[2][32];
+        tmem_ld32_nowait(tO + lane_base + c, v[0]);
+        tmem_ld32_nowait(tO + lane_base + c + 32, v[1]);
         tmem_wait_ld();
         if (row_valid) {
-          uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack16<BF16>(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[c / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack16<BF16>(__uint_as_float(v[h][2 * i]) * inv,
+                                  __uint_as_float(v[h][2 * i + 1]) * inv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[(c + 32 * h) / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
       }
       tc_fence_before();
