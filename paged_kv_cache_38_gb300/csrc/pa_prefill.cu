@@ -473,6 +473,45 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     const uint32_t lane_base = static_cast<uint32_t>((warp - kSoftmaxWarp0) * 32) << 16;
     int jx = 0;  // tiles processed, over all items
     bool ok = true;
+    // An item's epilogue (O / l to its rows, then O and the item slot released) is deferred
+    // into the next item's first tile, after that tile's weights are computed and its P is
+    // written: the wait for the item's last PV then overlaps useful work. O is complete there,
+    // since the wait for PV_{j-1} before writing P is the previous item's last PV.
+    bool pend = false, pend_valid = false;
+    float pend_inv = 0.f;
+    uint4* pend_dst = nullptr;
+    int pend_slot = 0;
+    auto epilogue = [&]() {
+      // two 32-column loads per wait: each tensor-memory round trip is on the item's path
+#pragma unroll 1
+      for (int c = 0; c < D; c += 64) {
+        uint32_t v[2][32];
+        tmem_ld32_nowait(tO + lane_base + c, v[0]);
+        tmem_ld32_nowait(tO + lane_base + c + 32, v[1]);
+        tmem_wait_ld();
+        if (pend_valid) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack16<BF16>(__uint_as_float(v[h][2 * i]) * pend_inv,
+                                  __uint_as_float(v[h][2 * i + 1]) * pend_inv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              pend_dst[(c + 32 * h) / 8 + i] =
+                  make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(o_free));
+        mbar_arrive(smem_addr(item_empty + pend_slot));
+      }
+      pend = false;
+    };
     for (int k = 0;; ++k) {
       const int slot = k % kSlots;
       ok = mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1);
@@ -604,6 +643,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         for (int c = 0; c < 8; ++c)
           *reinterpret_cast<uint4*>(prow + sw128_offset(r, c)) =
               make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        if (j == 0 && pend) epilogue();  // the previous item's O is complete (waited above)
         if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < D; c += 16) {
@@ -620,43 +660,20 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         if (lane == 0) mbar_arrive(smem_addr(p_full));
       }
       if (!ok) break;
-      // ---- epilogue of the item: O / l, then O is released to the next item's first PV
+      // ---- the item's epilogue is deferred (see above)
+      pend = true;
+      pend_valid = row_valid;
+      pend_inv = l > 0.f ? 1.f / l : 0.f;
+      pend_dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                          (static_cast<size_t>(it.q0 + tr) * Hq + it.g * G + r % G) * D);
+      pend_slot = slot;
+    }
+    if (ok && pend) {  // the last item's epilogue, once its last PV has completed
       ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1);
-      if (__any_sync(0xffffffffu, !ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(
-          static_cast<uint16_t*>(p.out) + (static_cast<size_t>(it.q0 + tr) * Hq + it.g * G + r % G) * D);
-      // two 32-column loads per wait: the epilogue stands between an item's last PV and the
-      // next item's first tile, so each tensor-memory round trip shows
-#pragma unroll 1
-      for (int c = 0; c < D; c += 64) {
-        uint32_t v[2][32];
-        tmem_ld32_nowait(tO + lane_base + c, v[0]);
-        tmem_ld32_nowait(tO + lane_base + c + 32, v[1]);
-        tmem_wait_ld();
-        if (row_valid) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              w[i] = pack16<BF16>(__uint_as_float(v[h][2 * i]) * inv,
-                                  __uint_as_float(v[h][2 * i + 1]) * inv);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[(c + 32 * h) / 8 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_addr(o_free));
-        mbar_arrive(smem_addr(item_empty + slot));
+      if (__any_sync(0xffffffffu, !ok)) ok = false;
+      if (ok) {
+        tc_fence_after();
+        epilogue();
       }
     }
     if (!ok && lane == 0) fail();
