@@ -82,6 +82,7 @@ struct WriteFp8Params {
   float k_scale, v_scale;
   int src_bf16;
   int num_tokens, num_kv_heads, chunks_per_row, block_size, num_blocks;
+  int log2_chunks, log2_block;  // when chunks_per_row and block_size are powers of two
 };
 
 // Two binary32 values to two E4M3 codes, nearest / ties-to-even, saturating to +-448 (NaN stays
@@ -117,34 +118,53 @@ __device__ __forceinline__ uint2 quantise8(uint4 w, float rcp, bool bf16) {
   return r;
 }
 
-// One thread per 16-element chunk of one (token, kv head) row.
+// Each thread converts two 16-element chunks of (token, kv head) rows per pass, both chunks'
+// loads issued before either is converted; the loads do not wait for the slot, only the stores
+// do. Index arithmetic is 32-bit (the host keeps a launch below 2^31 chunks), with shifts when
+// the row's chunk count and the block size are powers of two.
+template <bool kPow2>
 __global__ void __launch_bounds__(256) pa_write_kv_fp8_kernel(const __grid_constant__ WriteFp8Params p) {
-  const long long total =
-      static_cast<long long>(p.num_tokens) * p.num_kv_heads * p.chunks_per_row;
+  const uint32_t total = static_cast<uint32_t>(p.num_tokens) * p.num_kv_heads * p.chunks_per_row;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const uint32_t H = p.num_kv_heads, cpr = p.chunks_per_row, B = p.block_size;
   const bool bf16 = p.src_bf16 != 0;
   const float k_rcp = __frcp_rn(p.k_scale), v_rcp = __frcp_rn(p.v_scale);  // IEEE reciprocals
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(i % p.chunks_per_row);
-    const long long th = i / p.chunks_per_row;
-    const int h = static_cast<int>(th % p.num_kv_heads);
-    const int t = static_cast<int>(th / p.num_kv_heads);
-    const long long slot = __ldg(p.slots + t);
-    if (slot < 0) continue;  // padding token
-    const long long blk = slot / p.block_size;
-    if (blk >= p.num_blocks) {
-      if (h == 0 && c == 0) flag_error(p.err, kErrBlockId);
-      continue;
+  for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
+    uint4 kk[2][2], vv[2][2];
+    uint32_t th[2], c[2];
+    bool in[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t i = i0 + u * stride;
+      in[u] = i < total;
+      c[u] = kPow2 ? (i & (cpr - 1)) : i % cpr;
+      th[u] = kPow2 ? (i >> p.log2_chunks) : i / cpr;
+      if (in[u]) {
+        const size_t src = 2 * (static_cast<size_t>(th[u]) * cpr + c[u]);
+        kk[u][0] = __ldg(p.k + src);
+        kk[u][1] = __ldg(p.k + src + 1);
+        vv[u][0] = __ldg(p.v + src);
+        vv[u][1] = __ldg(p.v + src + 1);
+      }
     }
-    const long long src = 2 * (th * p.chunks_per_row + c);
-    const long long dst =
-        ((blk * p.num_kv_heads + h) * p.block_size + slot % p.block_size) * p.chunks_per_row + c;
-    const uint4 k0 = __ldg(p.k + src), k1 = __ldg(p.k + src + 1);
-    const uint4 v0 = __ldg(p.v + src), v1 = __ldg(p.v + src + 1);
-    const uint2 kq0 = quantise8(k0, k_rcp, bf16), kq1 = quantise8(k1, k_rcp, bf16);
-    const uint2 vq0 = quantise8(v0, v_rcp, bf16), vq1 = quantise8(v1, v_rcp, bf16);
-    p.k_pool[dst] = make_uint4(kq0.x, kq0.y, kq1.x, kq1.y);
-    p.v_pool[dst] = make_uint4(vq0.x, vq0.y, vq1.x, vq1.y);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!in[u]) continue;
+      const uint32_t t = th[u] / H, h = th[u] - t * H;
+      const long long slot = __ldg(p.slots + t);
+      if (slot < 0) continue;  // padding token
+      const long long blk = kPow2 ? (slot >> p.log2_block) : slot / B;
+      if (blk >= p.num_blocks) {
+        if (h == 0 && c[u] == 0) flag_error(p.err, kErrBlockId);
+        continue;
+      }
+      const long long off = kPow2 ? (slot & (B - 1)) : slot % B;
+      const size_t dst = ((static_cast<size_t>(blk) * H + h) * B + off) * cpr + c[u];
+      const uint2 kq0 = quantise8(kk[u][0], k_rcp, bf16), kq1 = quantise8(kk[u][1], k_rcp, bf16);
+      const uint2 vq0 = quantise8(vv[u][0], v_rcp, bf16), vq1 = quantise8(vv[u][1], v_rcp, bf16);
+      p.k_pool[dst] = make_uint4(kq0.x, kq0.y, kq1.x, kq1.y);
+      p.v_pool[dst] = make_uint4(vq0.x, vq0.y, vq1.x, vq1.y);
+    }
   }
 }
 
@@ -342,11 +362,31 @@ pa_status run_write_kv_fp8(const void* k, const void* v, pa_dtype src_dtype, voi
   p.chunks_per_row = head_dim / 16;
   p.block_size = block_size;
   p.num_blocks = num_blocks;
-  const long long total = static_cast<long long>(num_tokens) * num_kv_heads * p.chunks_per_row;
-  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256,
-                                                        std::max(1, device_sm_count()) * 8LL));
-  pa_write_kv_fp8_kernel<<<grid, 256, 0, stream>>>(p);
-  return cuda_status(cudaGetLastError(), "pa_write_kv_fp8 launch", msg);
+  auto log2_of = [](int x) { return (x & (x - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(x)) : -1; };
+  p.log2_chunks = log2_of(p.chunks_per_row);
+  p.log2_block = log2_of(block_size);
+  const bool pow2 = p.log2_chunks >= 0 && p.log2_block >= 0;
+  // launches of fewer than 2^31 chunks each (32-bit index arithmetic in the kernel)
+  const long long row_chunks = static_cast<long long>(num_kv_heads) * p.chunks_per_row;
+  const int max_tokens = static_cast<int>(std::max<long long>(1, ((1LL << 31) - 1) / row_chunks));
+  for (int t0 = 0; t0 < num_tokens; t0 += max_tokens) {
+    WriteFp8Params q = p;
+    q.num_tokens = std::min(max_tokens, num_tokens - t0);
+    q.k = p.k + 2 * static_cast<size_t>(t0) * row_chunks;
+    q.v = p.v + 2 * static_cast<size_t>(t0) * row_chunks;
+    q.slots = p.slots + t0;
+    const long long total = static_cast<long long>(q.num_tokens) * row_chunks;
+    const int grid = static_cast<int>(std::min<long long>((total + 511) / 512,
+                                                          std::max(1, device_sm_count()) * 8LL));
+    if (pow2) {
+      pa_write_kv_fp8_kernel<true><<<grid, 256, 0, stream>>>(q);
+    } else {
+      pa_write_kv_fp8_kernel<false><<<grid, 256, 0, stream>>>(q);
+    }
+    const pa_status st = cuda_status(cudaGetLastError(), "pa_write_kv_fp8 launch", msg);
+    if (st != PA_OK) return st;
+  }
+  return PA_OK;
 }
 
 pa_status run_copy_blocks(void* const* k_pools, void* const* v_pools, int32_t num_layers,
