@@ -96,6 +96,32 @@ def test_write_kv_fp8_every_bit_pattern(src):
         assert _nan_codes_agree(_u8(gv), exp_v), (src, vs)
 
 
+def test_write_kv_fp8_generic_geometry():
+    """A row of 3 chunks (head_dim 48), 12-token blocks and 3 kv heads (the kernel's division
+    path, not its power-of-two shifts), padding tokens, and enough tokens that threads make
+    more than one pass: the pools equal the oracle's byte for byte."""
+    orc = oracle.load()
+    D, B, H, ntok = 48, 12, 3, 70001
+    g = torch.Generator().manual_seed(11)
+    k = (torch.randn(ntok, H, D, generator=g) * 3).to(torch.bfloat16)
+    v = torch.randn(ntok, H, D, generator=g).to(torch.bfloat16)
+    nblk = ntok // B + 5
+    slots = torch.randperm(nblk * B, generator=g)[:ntok].to(torch.int64)
+    slots[::17] = -1
+    ks, vs = float(k.float().abs().max()) / 448.0, float(v.float().abs().max()) / 448.0
+    kp = torch.full((nblk, H, B, D), 0xAB, dtype=torch.uint8)
+    vp = torch.full((nblk, H, B, D), 0xCD, dtype=torch.uint8)
+    exp_k, exp_v = _u8(kp), _u8(vp)
+    assert orc.write_kv_fp8(k, v, exp_k, exp_v, slots, src_dtype="bf16", num_kv_heads=H,
+                            head_dim=D, block_size=B, k_scale=ks, v_scale=vs) == 0
+    gk, gv = kp.cuda(), vp.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_write_kv_fp8(k.cuda(), v.cuda(), gk, gv, slots.cuda(), ks, vs, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(_u8(gk), exp_k) and np.array_equal(_u8(gv), exp_v)
+
+
 def test_write_kv_fp8_then_decode():
     """A step on an E4M3 cache written by quantise-on-write: bit-exact pools (padding and an
     out-of-pool slot included), then the decode of the written cache matches the oracle."""
