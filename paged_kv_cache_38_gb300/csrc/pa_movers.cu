@@ -41,34 +41,54 @@ struct WriteParams {
   const int64_t* slots;
   int32_t* err;
   int num_tokens, num_kv_heads, chunks_per_row, block_size, num_blocks;
+  int log2_chunks, log2_block;  // when chunks_per_row and block_size are powers of two
 };
 
-// One thread per 16-byte chunk of one (token, kv head) row: pool[slot/B][h][slot%B][:] = new[t][h][:].
+// pool[slot/B][h][slot%B][:] = new[t][h][:], in 16-byte chunks of (token, kv head) rows. Each
+// thread moves two chunks per pass, both loads issued before either store; the loads do not wait
+// for the slot, only the stores do. Index arithmetic is 32-bit (the host keeps a launch below
+// 2^31 chunks), with shifts when the row's chunk count and the block size are powers of two.
+template <bool kPow2>
 __global__ void __launch_bounds__(256) pa_write_kv_kernel(const __grid_constant__ WriteParams p) {
-  const long long total =
-      static_cast<long long>(p.num_tokens) * p.num_kv_heads * p.chunks_per_row;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(i % p.chunks_per_row);
-    const long long th = i / p.chunks_per_row;
-    const int h = static_cast<int>(th % p.num_kv_heads);
-    const int t = static_cast<int>(th / p.num_kv_heads);
-    const long long slot = __ldg(p.slots + t);
-    if (slot < 0) continue;  // padding token
-    const long long blk = slot / p.block_size;
-    if (blk >= p.num_blocks) {
-      if (h == 0 && c == 0) flag_error(p.err, kErrBlockId);
-      continue;
+  const uint32_t total = static_cast<uint32_t>(p.num_tokens) * p.num_kv_heads * p.chunks_per_row;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const uint32_t H = p.num_kv_heads, cpr = p.chunks_per_row, B = p.block_size;
+  for (uint32_t i0 = blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
+    uint4 kk[2], vv[2];
+    uint32_t th[2], c[2];
+    bool in[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t i = i0 + u * stride;
+      in[u] = i < total;
+      c[u] = kPow2 ? (i & (cpr - 1)) : i % cpr;
+      th[u] = kPow2 ? (i >> p.log2_chunks) : i / cpr;
+      if (in[u]) {
+        const size_t src = static_cast<size_t>(th[u]) * cpr + c[u];
+        kk[u] = __ldg(p.k + src);
+        vv[u] = __ldg(p.v + src);
+      }
     }
-    const long long src = th * p.chunks_per_row + c;
-    const long long dst =
-        ((blk * p.num_kv_heads + h) * p.block_size + slot % p.block_size) * p.chunks_per_row + c;
-    const uint4 kv = __ldg(p.k + src);
-    const uint4 vv = __ldg(p.v + src);
-    p.k_pool[dst] = kv;
-    p.v_pool[dst] = vv;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (!in[u]) continue;
+      const uint32_t t = th[u] / H, h = th[u] - t * H;
+      const long long slot = __ldg(p.slots + t);
+      if (slot < 0) continue;  // padding token
+      const long long blk = kPow2 ? (slot >> p.log2_block) : slot / B;
+      if (blk >= p.num_blocks) {
+        if (h == 0 && c[u] == 0) flag_error(p.err, kErrBlockId);
+        continue;
+      }
+      const long long off = kPow2 ? (slot & (B - 1)) : slot % B;
+      const size_t dst = ((static_cast<size_t>(blk) * H + h) * B + off) * cpr + c[u];
+      p.k_pool[dst] = kk[u];
+      p.v_pool[dst] = vv[u];
+    }
   }
 }
+
+int log2_exact(int x) { return x > 0 && (x & (x - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(x)) : -1; }
 
 // ------------------------------------------------------------------ quantise-on-write (E4M3)
 
@@ -309,11 +329,30 @@ pa_status run_write_kv(const void* k, const void* v, void* k_pool, void* v_pool,
   p.chunks_per_row = head_dim * elt / 16;
   p.block_size = block_size;
   p.num_blocks = num_blocks;
-  const long long total = static_cast<long long>(num_tokens) * num_kv_heads * p.chunks_per_row;
-  const int grid = static_cast<int>(std::min<long long>((total + 255) / 256,
-                                                        std::max(1, device_sm_count()) * 8LL));
-  pa_write_kv_kernel<<<grid, 256, 0, stream>>>(p);
-  return cuda_status(cudaGetLastError(), "pa_write_kv launch", msg);
+  p.log2_chunks = log2_exact(p.chunks_per_row);
+  p.log2_block = log2_exact(block_size);
+  const bool pow2 = p.log2_chunks >= 0 && p.log2_block >= 0;
+  // launches of fewer than 2^31 chunks each (32-bit index arithmetic in the kernel)
+  const long long row_chunks = static_cast<long long>(num_kv_heads) * p.chunks_per_row;
+  const int max_tokens = static_cast<int>(std::max<long long>(1, ((1LL << 31) - 1) / row_chunks));
+  for (int t0 = 0; t0 < num_tokens; t0 += max_tokens) {
+    WriteParams q = p;
+    q.num_tokens = std::min(max_tokens, num_tokens - t0);
+    q.k = p.k + static_cast<size_t>(t0) * row_chunks;
+    q.v = p.v + static_cast<size_t>(t0) * row_chunks;
+    q.slots = p.slots + t0;
+    const long long total = static_cast<long long>(q.num_tokens) * row_chunks;
+    const int grid = static_cast<int>(std::min<long long>((total + 511) / 512,
+                                                          std::max(1, device_sm_count()) * 8LL));
+    if (pow2) {
+      pa_write_kv_kernel<true><<<grid, 256, 0, stream>>>(q);
+    } else {
+      pa_write_kv_kernel<false><<<grid, 256, 0, stream>>>(q);
+    }
+    const pa_status st = cuda_status(cudaGetLastError(), "pa_write_kv launch", msg);
+    if (st != PA_OK) return st;
+  }
+  return PA_OK;
 }
 
 pa_status run_write_kv_fp8(const void* k, const void* v, pa_dtype src_dtype, void* k_pool,
@@ -362,9 +401,8 @@ pa_status run_write_kv_fp8(const void* k, const void* v, pa_dtype src_dtype, voi
   p.chunks_per_row = head_dim / 16;
   p.block_size = block_size;
   p.num_blocks = num_blocks;
-  auto log2_of = [](int x) { return (x & (x - 1)) == 0 ? __builtin_ctz(static_cast<unsigned>(x)) : -1; };
-  p.log2_chunks = log2_of(p.chunks_per_row);
-  p.log2_block = log2_of(block_size);
+  p.log2_chunks = log2_exact(p.chunks_per_row);
+  p.log2_block = log2_exact(block_size);
   const bool pow2 = p.log2_chunks >= 0 && p.log2_block >= 0;
   // launches of fewer than 2^31 chunks each (32-bit index arithmetic in the kernel)
   const long long row_chunks = static_cast<long long>(num_kv_heads) * p.chunks_per_row;

@@ -48,6 +48,31 @@ def test_write_kv_bit_exact(spec):
     assert np.array_equal(_u8(gk), exp_k) and np.array_equal(_u8(gv), exp_v)
 
 
+def test_write_kv_generic_geometry():
+    """bf16 rows of 6 chunks (head_dim 48), 12-token blocks, 3 kv heads (the kernel's division
+    path), padding tokens, and enough tokens that threads make more than one pass: the pools
+    equal the oracle's byte for byte."""
+    orc = oracle.load()
+    D, B, H, ntok = 48, 12, 3, 40001
+    g = torch.Generator().manual_seed(12)
+    k = torch.randn(ntok, H, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(ntok, H, D, generator=g).to(torch.bfloat16)
+    nblk = ntok // B + 5
+    slots = torch.randperm(nblk * B, generator=g)[:ntok].to(torch.int64)
+    slots[::13] = -1
+    kp = torch.full((nblk, H, B, D), 7.0, dtype=torch.bfloat16)
+    vp = torch.full((nblk, H, B, D), -3.0, dtype=torch.bfloat16)
+    exp_k, exp_v = _u8(kp), _u8(vp)
+    assert orc.write_kv(k, v, exp_k, exp_v, slots, num_kv_heads=H, head_dim=D, block_size=B,
+                        kv_dtype="bf16") == 0
+    gk, gv = kp.cuda(), vp.cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_write_kv(k.cuda(), v.cuda(), gk, gv, slots.cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.array_equal(_u8(gk), exp_k) and np.array_equal(_u8(gv), exp_v)
+
+
 def test_write_kv_out_of_pool_flagged():
     spec = synth.SPECS["toy"]
     case = synth.make_case(spec, seed=1).to("cuda")
