@@ -22,12 +22,15 @@
 //     2-stage ring;
 //   * warp 1 allocates tensor memory and one lane issues the MMAs: S_j = Q K_j^T (M 128, N 64)
 //     into one of two TMEM S buffers, and O += P_j V_j (M 128, N = head_dim) into the TMEM O
-//     accumulator; one tcgen05.commit per MMA group signals its completion on an mbarrier,
-//     which also hands the group's K (or V) stage back to its producer;
+//     accumulator, PV first when both are ready; one tcgen05.commit per MMA group signals its
+//     completion on an mbarrier, which also hands the group's K (or V) stage back to its
+//     producer;
 //   * warps 4-7 (one thread per row) read S with tcgen05.ld, apply the causal mask and the
-//     online softmax (log2 domain), write P (16-bit, swizzled K-major) to shared memory and
-//     rescale O in tensor memory when a row's running maximum grows; at the end of an item they
-//     divide O by the row sums and store the rows.
+//     online softmax (log2 domain, packed fp32 pairs), write P (16-bit, swizzled K-major) to
+//     shared memory and rescale O in tensor memory when a row's running maximum grows; an
+//     item's epilogue (O divided by the row sums, rows stored) runs inside the next item's
+//     first tile, once that tile's P is written, so that the wait for the item's last PV
+//     overlaps the next tile's softmax.
 // Every wait is bounded; on a timeout the CTA flags PA_ERR_TIMEOUT, the roles wind down, the
 // MMAs drain through one last commit and the tensor memory is freed before the CTA returns.
 #include <cuda_bf16.h>
