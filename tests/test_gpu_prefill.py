@@ -70,6 +70,35 @@ def test_prefill_long_chunks():
     assert _err(out, ref) <= TOL["bf16"]
 
 
+def test_prefill_growing_scores_rescale():
+    """Scores that grow along the context (each key row scaled by 1 + position / 100): every
+    row's running maximum passes the lazy-rescaling threshold several times, so O is rescaled
+    in tensor memory, and the result still matches the oracle (V scaled down so that outputs
+    stay below 1 and bf16 output rounding stays far inside the tolerance)."""
+    spec = synth.DecodeSpec("pf_grow", 3, 16, 4, 128, 16, "bf16", "bf16", ctx_lens=(700, 400, 1000))
+    case = synth.make_case(spec, seed=72)
+    bt, lens = case.block_tables.numpy(), case.ctx_lens.numpy()
+    kp, vp = case.k_pool, case.v_pool
+    done = set()
+    for si in range(spec.num_seqs):
+        for t in range(int(lens[si])):
+            blk, off = int(bt[si, t // spec.block_size]), t % spec.block_size
+            if (blk, off) in done:
+                continue
+            done.add((blk, off))
+            kp[blk, :, off] = (kp[blk, :, off].float() * (1.0 + t / 100.0)).to(kp.dtype)
+            vp[blk, :, off] = (vp[blk, :, off].float() * 0.25).to(vp.dtype)
+    qs, q = synth.prefill_queries(case, seed=8, whole=True)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qs.cuda(),
+                        case.scale, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _err(out, ref) <= TOL["bf16"]
+
+
 def test_prefill_bad_lengths_flagged():
     spec = synth.DecodeSpec("pf_bad", 3, 8, 2, 128, 16, "bf16", "bf16", ctx_lens=(40, 40, 40))
     case = synth.make_case(spec, seed=5).to("cuda")
