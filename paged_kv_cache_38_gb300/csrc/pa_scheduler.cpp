@@ -21,6 +21,7 @@ struct Seq {
   std::vector<int32_t> table;  // GPU blocks (CPU slots while swapped)
   int32_t length = 0;          // KV positions stored
   int32_t generated = 0;       // tokens produced
+  int32_t row = -1;            // batch row in the last plan
 };
 
 struct Group {
@@ -55,7 +56,11 @@ struct pa_scheduler {
 
   // the last plan's storage
   std::vector<int64_t> seq_ids, finished, preempted, slots;
-  std::vector<int32_t> tables, ctx_lens, write_seq, write_pos, copies, swap_out, swap_in;
+  std::vector<int32_t> ctx_lens, write_seq, write_pos, copies, swap_out, swap_in;
+  // The plan's block tables persist across steps: row i holds row_len[i] entries and -1 after
+  // them, so a step rewrites each row's entries and clears only what its old length covered
+  // beyond the new one, instead of all max_blocks entries of every row.
+  std::vector<int32_t> tables, row_len;
 
   int32_t alloc_gpu() {
     const int32_t b = free_gpu.front();
@@ -113,7 +118,6 @@ struct pa_scheduler {
     finished.clear();
     preempted.clear();
     slots.clear();
-    tables.clear();
     ctx_lens.clear();
     write_seq.clear();
     write_pos.clear();
@@ -260,21 +264,25 @@ struct pa_scheduler {
     }
 
     // 5. the batch
-    std::unordered_map<const Seq*, int32_t> index;
     const int64_t n = running_seqs();
-    tables.resize(static_cast<size_t>(n) * max_blocks);
-    int32_t* row = tables.data();
-    for (const Group* g : running)
-      for (const Seq& s : g->seqs) {
-        index[&s] = static_cast<int32_t>(seq_ids.size());
+    if (static_cast<int64_t>(row_len.size()) < n) {
+      tables.resize(static_cast<size_t>(n) * max_blocks, -1);
+      row_len.resize(static_cast<size_t>(n), 0);
+    }
+    for (Group* g : running)
+      for (Seq& s : g->seqs) {
+        const int32_t i = static_cast<int32_t>(seq_ids.size());
+        s.row = i;
         seq_ids.push_back(g->id * 256 + s.sample);
+        int32_t* row = tables.data() + static_cast<size_t>(i) * max_blocks;
+        const int32_t len = static_cast<int32_t>(s.table.size());
         std::copy(s.table.begin(), s.table.end(), row);
-        std::fill(row + s.table.size(), row + max_blocks, -1);
-        row += max_blocks;
+        if (len < row_len[i]) std::fill(row + len, row + row_len[i], -1);
+        row_len[i] = len;
         ctx_lens.push_back(s.length);
       }
     for (const Write& w : writes) {
-      write_seq.push_back(index.at(w.seq));
+      write_seq.push_back(w.seq->row);
       write_pos.push_back(w.pos);
       slots.push_back(w.slot);
     }
