@@ -50,9 +50,11 @@ def _bind(L) -> None:
 
 
 def _arr(ptr, n, dtype) -> np.ndarray:
-    if n == 0:
-        return np.zeros(0, dtype=dtype)
-    return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dtype, copy=True)
+    """A copy of n elements at ptr (one memmove into a new array)."""
+    out = np.empty(n, dtype=dtype)
+    if n:
+        ctypes.memmove(out.ctypes.data, ptr, out.nbytes)
+    return out
 
 
 class Plan:
