@@ -11,7 +11,7 @@
 //   * Work items are (sequence, kv head, context split) in sequence order; CTAs take the next
 //     item from a global counter, so the items of sequences that share prompt blocks run at the
 //     same time on different SMs and the shared blocks are served from L2.
-//   * Warp 0 schedules: it keeps up to 4 items queued in shared memory -- descriptor, the
+//   * Warp 0 schedules: it keeps up to 2 items queued in shared memory -- descriptor, the
 //     item's block-table slice (one coalesced load, out-of-pool ids masked and flagged) and the
 //     group's queries (one bulk copy).
 //   * Warps 1..4 produce: tile g of the CTA's tile sequence is issued by warp 1 + g % 4 as 2-D
