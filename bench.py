@@ -39,6 +39,9 @@ import synth  # noqa: E402
 WORKLOAD = "gqa_pressure"
 SEED = 38 + 2  # seed = 38 + index of the configuration
 METRIC = "paged-decode attention: achieved HBM GB/s & % of peak; decode tokens/s"
+# GB300 HBM3e bandwidth from NVIDIA's public specification, entered by hand: the "nominal" peak
+# printed beside the measured copy peak of MEASURED_PEAKS.json.
+NOMINAL_HBM_GBS = 7900.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.txt")
 DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh", "pa_decode_host.cu", "pa_decode_bf16.cu"]
 
@@ -362,6 +365,7 @@ def run_ours(args, world, rank, local) -> None:
         "data": "synthetic (seeded block pools shaped like the pages' workloads)",
         "config": workload_config(args.workload, spec, case, split, world),
         "pct_of_peak": round(100 * value / world / peaks["hbm_gbs"], 1),
+        "pct_of_nominal": round(100 * value / world / NOMINAL_HBM_GBS, 1),
         "decode_tokens_per_s": round(world * spec.num_seqs / (ms_per_step * 1e-3), 1),
         "ms_per_step_eager": round(eager_ms, 4),
         "bytes_per_step": {**dbytes, **mbytes, "total": step_bytes},
@@ -369,6 +373,9 @@ def run_ours(args, world, rank, local) -> None:
                      "achieved": round(dec_gbs, 1), "peak": peaks["hbm_gbs"],
                      "peak_source": peaks["source"], "unit": "GB/s",
                      "frac": round(dec_gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "nominal": {"peak": NOMINAL_HBM_GBS, "unit": "GB/s",
+                                 "frac": round(dec_gbs / NOMINAL_HBM_GBS, 4),
+                                 "source": "GB300 HBM3e specification (nominal)"},
                      "algorithmic_bytes": dbytes["total"], "ms_per_launch": round(dec_ms, 4)},
         "gpu_launches": step.launches * args.steps,
         "clocks": clocks.summary(),
@@ -456,6 +463,7 @@ def run_extras(args, dev, flush, peaks) -> dict:
         b = decode_bytes(case, split)
         res[name] = {"decode_ms": round(t, 4), "gbs": round(b["total"] / (t * 1e-3) / 1e9, 1),
                      "pct_of_peak": round(100 * b["total"] / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 1),
+                     "pct_of_nominal": round(100 * b["total"] / (t * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
                      "tokens_per_s": round(spec.num_seqs / (t * 1e-3), 1),
                      "split_tokens": split, "bytes": b["total"]}
         del case, st
@@ -731,12 +739,12 @@ def run_swap_bench(dev) -> dict:
     return res
 
 
-def run_copy_bench(dev, flush, peaks) -> dict:
+def run_copy_bench(dev, flush, peaks, layers: int = 32) -> dict:
     """pa_copy_blocks at the preemption geometry: 4,096 disjoint pairs x 32 layers, plus the
     25-pair step of the GQA workload as a latency figure."""
     import paged_kv_cache_38_gb300 as pa
 
-    layers, nblk, bb = 32, 8192 + 64, 32 * 1024
+    nblk, bb = 8192 + 64, 32 * 1024
     k = [torch.empty(nblk, bb, dtype=torch.uint8, device=dev) for _ in range(layers)]
     v = [torch.empty(nblk, bb, dtype=torch.uint8, device=dev) for _ in range(layers)]
     perm = torch.from_numpy(np.random.default_rng(SEED).permutation(nblk)[:8192].astype(np.int32))
@@ -758,8 +766,9 @@ def run_copy_bench(dev, flush, peaks) -> dict:
 # ---------------------------------------------------------------------------- CPU oracle
 
 def cpu_baseline(case: synth.PagedCase, split: int, seconds: float) -> dict:
-    """The fp64 oracle as it stands, on all host cores, over a seeded sample of the step's
-    sequences (whole step: write, copy, decode), scaled to the same GB/s metric."""
+    """The fp64 oracle as it stands over a seeded sample of the step's sequences (whole step:
+    write, copy, decode), scaled to the same GB/s metric: on all host cores (the line's value)
+    and on one core, each for about ``seconds``."""
     import oracle
 
     orc = oracle.load()
@@ -768,26 +777,36 @@ def cpu_baseline(case: synth.PagedCase, split: int, seconds: float) -> dict:
     vp = case.v_pool.cpu().view(torch.uint8).numpy().reshape(-1).copy()
     q = case.q.cpu()
     bt, cl = case.block_tables.cpu(), case.ctx_lens.cpu()
-    rng = np.random.default_rng(SEED)
-    order = rng.permutation(spec.num_seqs)
-    done, t0, byts = 0, time.perf_counter(), 0
     row = spec.num_kv_heads * spec.head_dim * synth.ELT_BYTES[spec.kv_dtype]
-    orc.write_kv(case.k_new.cpu(), case.v_new.cpu(), kp, vp, case.slot_mapping.cpu(),
-                 num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
-                 block_size=spec.block_size, kv_dtype=spec.kv_dtype)
-    while done < spec.num_seqs and time.perf_counter() - t0 < seconds:
-        idx = torch.as_tensor(order[done:done + 4], dtype=torch.long)
-        orc.decode(q[idx], kp, vp, bt[idx], cl[idx], q_dtype=spec.q_dtype,
-                   kv_dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
-                   num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
-                   block_size=spec.block_size, scale=case.scale)
-        byts += 2 * row * int(cl[idx].sum()) + 2 * len(idx) * spec.num_q_heads * spec.head_dim * 2
-        done += len(idx)
-    el = time.perf_counter() - t0
-    return {"value": round(byts / el / 1e9, 3), "unit": "GB/s", "cores": orc.max_threads(),
-            "kind": "oracle", "seconds": round(el, 2),
-            "sample": f"write_kv of the step + oracle decode of {done} of {spec.num_seqs} "
-                      f"sequences (seeded order), logical KV bytes per second"}
+
+    def rate(threads: int, chunk: int) -> dict:
+        order = np.random.default_rng(SEED).permutation(spec.num_seqs)
+        done, t0, byts = 0, time.perf_counter(), 0
+        orc.write_kv(case.k_new.cpu(), case.v_new.cpu(), kp, vp, case.slot_mapping.cpu(),
+                     num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                     block_size=spec.block_size, kv_dtype=spec.kv_dtype)
+        byts += 2 * 2 * row * spec.num_seqs
+        while done < spec.num_seqs and time.perf_counter() - t0 < seconds:
+            idx = torch.as_tensor(order[done:done + chunk], dtype=torch.long)
+            orc.decode(q[idx], kp, vp, bt[idx], cl[idx], q_dtype=spec.q_dtype,
+                       kv_dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
+                       num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
+                       block_size=spec.block_size, scale=case.scale, num_threads=threads)
+            byts += (2 * row * int(cl[idx].sum())
+                     + 2 * len(idx) * spec.num_q_heads * spec.head_dim * 2)
+            done += len(idx)
+        el = time.perf_counter() - t0
+        return {"value": round(byts / el / 1e9, 3), "seconds": round(el, 2), "seqs": done}
+
+    cores = orc.max_threads()
+    allc = rate(0, 4)
+    one = rate(1, 1)
+    sample = ("write_kv of the step + oracle decode of {n} of %d sequences (seeded order), "
+              "KV, q and output bytes per second" % spec.num_seqs)
+    return {"value": allc["value"], "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "seconds": allc["seconds"], "sample": sample.format(n=allc["seqs"]),
+            "single_thread": {"value": one["value"], "unit": "GB/s", "cores": 1,
+                              "seconds": one["seconds"], "sample": sample.format(n=one["seqs"])}}
 
 
 def workload_config(name: str, spec: synth.DecodeSpec, case: synth.PagedCase, split: int,
@@ -880,9 +899,19 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="time budget of the reference arm's warm-up and timed steps")
+    ap.add_argument("--copy-only-layers", type=int, default=0,
+                    help="run only the 4,096-pair pa_copy_blocks bench with this many layers "
+                         "(a small case for profiling) and print its result")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.copy_only_layers > 0:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+        print(json.dumps(run_copy_bench(dev, flush, load_peaks(), layers=args.copy_only_layers)))
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)

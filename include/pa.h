@@ -294,14 +294,36 @@ pa_status pa_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t num
  *   - It allocates nothing. A decode whose pa_decode_workspace_size() exceeds
  *     PA_STATIC_WORKSPACE_BYTES is rejected with PA_EINVAL (raise split_tokens, or use
  *     pa_decode with a workspace of your own).
- *   - The first call on a device looks up the array's device address (once per device); make
- *     that first call before any stream capture.
+ *   - The first call on a device looks up the array's device address (once per device and
+ *     CUDA context: again after a device reset); make that first call before any stream
+ *     capture.
  *   - Every call on a device shares the one array, which keeps whatever the last call left in
  *     it (the kernel needs no zeroed scratch). Calls that may overlap on the GPU -- on different
  *     streams, or from different host threads -- race on it and must be serialised by the caller.
  */
 #define PA_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 pa_status pa_decode_static_workspace(const pa_decode_args* args, pa_stream stream);
+
+/*
+ * pa_testing_set_wait_limit - make the kernels' bounded waits run out (tests only).
+ *
+ * Not an operation of the pages: it exists so that tests can show that a kernel gives up
+ * cleanly. Every wait of one warp, role or CTA on another inside pa_decode and pa_prefill is
+ * bounded; when it expires the kernel sets PA_ERR_TIMEOUT, waits for its own copies and tensor
+ * core operations still in flight, frees its tensor memory, leaves pa_decode's work counters
+ * cleared for the next launch and returns (the outputs of that call are unspecified).
+ *   wait_ns    limit of those waits in nanoseconds for launches enqueued from now on;
+ *              0 restores the default of one second. Waits for a kernel's own copies keep
+ *              their one-second limit.
+ *   stall_cta  -1: no effect. Otherwise the CTA with this index withholds its part, so that
+ *              the others' waits on it must run out: in pa_decode it does not arrive at the
+ *              grid-wide barrier before the split-K combine (only launches with more than one
+ *              split reach that barrier); in pa_prefill its MMA issuer stops after its first
+ *              S = Q K^T group.
+ * The setting is process-wide, is read when a call is enqueued (a captured CUDA graph keeps
+ * the setting it was captured with) and is not thread-safe with respect to concurrent calls.
+ */
+pa_status pa_testing_set_wait_limit(uint64_t wait_ns, int32_t stall_cta);
 
 /* Static description of a status code. */
 const char* pa_status_string(pa_status status);

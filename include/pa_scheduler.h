@@ -3,7 +3,8 @@
  *
  * It plans, step by step, what the kernels of pa.h do: which sequences run, their block
  * tables and context lengths, the slot of every KV position written, the copy-on-write pairs
- * and the blocks swapped to and from CPU memory. Host memory only; no CUDA call.
+ * and the blocks swapped to and from CPU memory. Planning uses host memory only and makes no
+ * CUDA call; pa_scheduler_execute_moves enqueues a plan's block moves on the GPU.
  *
  * Sources:
  *   "When KV Capacity Runs Out: Pausing and Resuming Requests", Figures 1-5: a block is linked
@@ -41,7 +42,8 @@
  * yields one token for every sequence in the batch.
  *
  * The caller executes a plan in this order: swap-outs (GPU block -> CPU slot), swap-ins
- * (CPU slot -> GPU block), copy-on-write copies, KV writes (slot_mapping), decode.
+ * (CPU slot -> GPU block), copy-on-write copies (the three by pa_scheduler_execute_moves), KV
+ * writes (slot_mapping), decode.
  *
  * Ownership: a scheduler owns the arrays of the plan it last returned; they stay valid until
  * its next step or its destruction. Calls on one scheduler must not overlap.
@@ -49,6 +51,7 @@
 #ifndef PA_SCHEDULER_H
 #define PA_SCHEDULER_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #include "pa.h"
@@ -110,6 +113,36 @@ int32_t pa_scheduler_free_blocks(const pa_scheduler* s, int32_t* out, int32_t ca
 
 /* 1 while some request is waiting or running, else 0. */
 int32_t pa_scheduler_has_unfinished(const pa_scheduler* s);
+
+/*
+ * pa_scheduler_execute_moves - enqueue a plan's block moves, in the order the plan requires.
+ *
+ * Sources: "When KV Capacity Runs Out", Figure 4 (a preempted request's KV goes to CPU memory
+ * before its blocks are reused, and comes back into possibly different blocks); PagedAttention
+ * summary page, copy-on-write paragraph. Enqueues on `stream`, in this order:
+ *   1. swap-outs:  for each (GPU block b, CPU slot c) of plan->swap_out, every layer l:
+ *                  cpu_pool[c][l][0][:] = k_pools[l][b][...], cpu_pool[c][l][1][:] = v_pools[l][b]
+ *   2. swap-ins:   for each (CPU slot c, GPU block b) of plan->swap_in: the reverse assignment;
+ *   3. copies:     for each (src, dst) of plan->copies: every layer's K and V block dst
+ *                  becomes a copy of block src (pa_copy_blocks semantics).
+ * The plan's lists are read on the host during the call (nothing is uploaded: the ids travel
+ * as kernel parameters), so the plan may be released or re-planned as soon as this returns.
+ * The KV writes (pa_write_kv with plan->slot_mapping) and the decode are the caller's: they
+ * need this step's new K/V and queries.
+ *   k_pools, v_pools  host arrays of num_layers device pool pointers, each
+ *                     [num_blocks][block_bytes] (16-byte aligned)
+ *   cpu_pool          pinned host memory [num_cpu_blocks][num_layers][2][block_bytes]
+ *                     (16-byte aligned; may be NULL when the plan has no swaps)
+ *   err_flag          optional device int32 (as in pa.h; host-checked ids cannot set it)
+ * Errors: PA_EINVAL, with nothing enqueued, if a block id lies outside [0, num_blocks), a CPU
+ * slot outside [0, num_cpu_blocks), or cpu_pool is not pinned; PA_ECUDA if a launch fails. The
+ * caller must not reuse swapped-out GPU blocks, or overwrite swapped-in CPU slots, until the
+ * stream has passed this call.
+ */
+pa_status pa_scheduler_execute_moves(const pa_step_plan* plan, void* const* k_pools,
+                                     void* const* v_pools, int32_t num_layers, int32_t num_blocks,
+                                     size_t block_bytes, void* cpu_pool, int32_t num_cpu_blocks,
+                                     int32_t* err_flag, pa_stream stream);
 
 #ifdef __cplusplus
 }

@@ -98,8 +98,8 @@ class Oracle:
                                         ctypes.c_size_t, _c_int]
         lib.pao_max_threads.restype = _c_int
         lib.pao_prefill.restype = _c_int
-        lib.pao_prefill.argtypes = [_ptr, _ptr, _ptr, _c_int, _ptr, _ptr, _ptr] + [_c_int] * 7 + [
-            _c_dbl, _ptr, _c_int]
+        lib.pao_prefill.argtypes = [_ptr, _c_int, _ptr, _ptr, _c_int, _ptr, _ptr, _ptr] + [
+            _c_int] * 7 + [_c_dbl, _c_dbl, _c_dbl, _ptr, _c_int]
         lib.pao_e4m3_encode_array.restype = None
         lib.pao_e4m3_encode_array.argtypes = [_ptr, _ptr, ctypes.c_size_t]
         lib.pao_write_kv_fp8.restype = _c_int
@@ -150,9 +150,11 @@ class Oracle:
 
     def prefill(self, q, k_pool, v_pool, block_tables, ctx_lens, q_starts, *, dtype: str,
                 num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
-                scale: float, num_threads: int = 0, return_status: bool = False):
+                scale: float, q_dtype: Optional[str] = None, k_scale: float = 1.0,
+                v_scale: float = 1.0, num_threads: int = 0, return_status: bool = False):
         """fp64 causal attention of each sequence's chunk of query tokens over its paged cache:
-        [num_tokens][num_q_heads][head_dim]."""
+        [num_tokens][num_q_heads][head_dim]. ``dtype`` is the KV dtype; the queries have
+        ``q_dtype`` (default: the KV dtype); an E4M3 cache is read as stored value x scale."""
         qb, kb, vb = _raw(q), _raw(k_pool), _raw(v_pool)
         cl = _int_array(ctx_lens, np.int32).reshape(-1)
         qs = _int_array(q_starts, np.int32).reshape(-1)
@@ -161,10 +163,10 @@ class Oracle:
         per_block = num_kv_heads * block_size * head_dim * ELT_BYTES[dtype]
         ntok = int(qs[-1]) if qs.size else 0
         out = np.zeros((ntok, num_q_heads, head_dim), dtype=np.float64)
-        rc = self.lib.pao_prefill(_p(qb), _p(kb), _p(vb), DTYPES[dtype], _p(bt), _p(cl), _p(qs), n,
-                                  num_q_heads, num_kv_heads, head_dim, block_size,
-                                  kb.size // per_block, bt.shape[1], float(scale), _p(out),
-                                  int(num_threads))
+        rc = self.lib.pao_prefill(_p(qb), DTYPES[q_dtype or dtype], _p(kb), _p(vb), DTYPES[dtype],
+                                  _p(bt), _p(cl), _p(qs), n, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, kb.size // per_block, bt.shape[1], float(scale),
+                                  float(k_scale), float(v_scale), _p(out), int(num_threads))
         return (out, rc) if return_status else out
 
     # -------------------------------------------------------------- block movers

@@ -252,14 +252,17 @@ int pao_decode(const void* q, int q_dtype, const void* k_pool, const void* v_poo
  * query tokens, q rows q_starts[s] .. q_starts[s + 1] - 1, and query i stands at position
  * L - n + i. For each query head h (kv group g = h / (Hq / Hkv)):
  *   s_t = scale * sum_d q[h][d] * K^[t][d]  for t <= L - n + i;  out = sum_t softmax(s)_t V^[t],
- * with K^, V^ gathered through the block table as in pao_decode. Returns 0, or -1 if some
- * length or block id is invalid (those rows are zero).
+ * with K^, V^ gathered through the block table as in pao_decode: for an FP8 cache ([PV]
+ * section "How much KV cache a token costs") K^ = k_scale * the stored E4M3 value and
+ * V^ = v_scale * the stored value, so a recomputed request can be prefilled over the same
+ * one-byte cache its decode steps read. Returns 0, or -1 if some length or block id is invalid
+ * (those rows are zero).
  */
-int pao_prefill(const void* q, const void* k_pool, const void* v_pool, int dtype,
+int pao_prefill(const void* q, int q_dtype, const void* k_pool, const void* v_pool, int kv_dtype,
                 const int32_t* block_tables, const int32_t* ctx_lens, const int32_t* q_starts,
                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                int num_blocks, int max_blocks_per_seq, double scale, double* out,
-                int num_threads) {
+                int num_blocks, int max_blocks_per_seq, double scale, double k_scale,
+                double v_scale, double* out, int num_threads) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return -1;
   const int group = num_q_heads / num_kv_heads;
   int bad = 0;
@@ -295,8 +298,8 @@ int pao_prefill(const void* q, const void* k_pool, const void* v_pool, int dtype
         const size_t first =
             (((size_t)phys * num_kv_heads + g) * block_size + t % block_size) * head_dim;
         for (int d = 0; d < head_dim; ++d) {
-          K[(size_t)t * head_dim + d] = element(k_pool, first + d, dtype);
-          V[(size_t)t * head_dim + d] = element(v_pool, first + d, dtype);
+          K[(size_t)t * head_dim + d] = k_scale * element(k_pool, first + d, kv_dtype);
+          V[(size_t)t * head_dim + d] = v_scale * element(v_pool, first + d, kv_dtype);
         }
       }
       if (!rows_ok) {
@@ -315,7 +318,7 @@ int pao_prefill(const void* q, const void* k_pool, const void* v_pool, int dtype
         for (int t = 0; t <= last; ++t) {
           double dot = 0.0;
           for (int d = 0; d < head_dim; ++d)
-            dot += element(q, qoff + d, dtype) * K[(size_t)t * head_dim + d];
+            dot += element(q, qoff + d, q_dtype) * K[(size_t)t * head_dim + d];
           score[t] = scale * dot;
           if (score[t] > max_score) max_score = score[t];
         }

@@ -6,11 +6,12 @@ attention and the KV block movers; ``pa`` marshals torch tensors into its C entr
 from .pa import (PA_BF16, PA_ECUDA, PA_EINVAL, PA_ERR_BLOCK_ID, PA_ERR_CTX_LEN, PA_ERR_TIMEOUT,
                  PA_EUNSUPPORTED, PA_F16, PA_FP8_E4M3, PA_OK, PA_SWAP_IN, PA_SWAP_OUT, PaError,
                  lib, make_decode_args, pa_copy_blocks, pa_decode, pa_decode_workspace_size,
-                 pa_prefill, pa_swap_blocks, pa_write_kv, pa_write_kv_fp8)
+                 pa_prefill, pa_swap_blocks, pa_testing_set_wait_limit, pa_write_kv,
+                 pa_write_kv_fp8)
 
 __all__ = [
     "PA_BF16", "PA_ECUDA", "PA_EINVAL", "PA_ERR_BLOCK_ID", "PA_ERR_CTX_LEN", "PA_ERR_TIMEOUT",
     "PA_EUNSUPPORTED", "PA_F16", "PA_FP8_E4M3", "PA_OK", "PA_SWAP_IN", "PA_SWAP_OUT", "PaError",
     "lib", "make_decode_args", "pa_copy_blocks", "pa_decode", "pa_decode_workspace_size",
-    "pa_prefill", "pa_swap_blocks", "pa_write_kv", "pa_write_kv_fp8",
+    "pa_prefill", "pa_swap_blocks", "pa_testing_set_wait_limit", "pa_write_kv", "pa_write_kv_fp8",
 ]

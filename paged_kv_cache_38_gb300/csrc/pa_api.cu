@@ -2,6 +2,7 @@
 //
 // Each entry point validates its arguments on the host, enqueues its kernels on the caller's
 // stream and returns; no call allocates, frees or synchronises.
+#include <atomic>
 #include <string>
 
 #include "pa_internal.h"
@@ -9,6 +10,10 @@
 namespace {
 
 thread_local std::string g_last_error;
+
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // one second
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_stall_cta{-1};
 
 pa_status finish(pa_status st, const std::string& msg) {
   if (st != PA_OK) g_last_error = msg.empty() ? pa_status_string(st) : msg;
@@ -19,6 +24,8 @@ pa_status finish(pa_status st, const std::string& msg) {
 
 namespace pa {
 pa_status record_error(pa_status st, const std::string& msg) { return finish(st, msg); }
+unsigned long long launch_wait_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+int launch_stall_cta() { return g_stall_cta.load(std::memory_order_relaxed); }
 }  // namespace pa
 
 extern "C" {
@@ -40,6 +47,14 @@ const char* pa_status_string(pa_status status) {
 }
 
 const char* pa_last_error_message(void) { return g_last_error.c_str(); }
+
+pa_status pa_testing_set_wait_limit(uint64_t wait_ns, int32_t stall_cta) {
+  if (stall_cta < -1) return finish(PA_EINVAL, "stall_cta must be -1 or a CTA index");
+  g_wait_ns.store(wait_ns == 0 ? kDefaultWaitNs : static_cast<unsigned long long>(wait_ns),
+                  std::memory_order_relaxed);
+  g_stall_cta.store(stall_cta, std::memory_order_relaxed);
+  return PA_OK;
+}
 
 size_t pa_decode_workspace_size(const pa_decode_args* args) {
   std::string msg;

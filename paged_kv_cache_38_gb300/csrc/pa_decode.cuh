@@ -83,6 +83,9 @@ struct DecodeParams {
   float score_scale;    // scale * k_scale * log2(e)
   float v_scale;
   int q_bf16;           // query / output dtype is bf16 (else f16)
+  unsigned long long wait_ns;  // limit of a wait on another warp or CTA (1 s unless a test
+                               // shortened it)
+  int stall_cta;        // testing: this CTA withholds its grid-barrier arrival (-1: none)
 };
 
 // Work item handed from the scheduler warp to the producers and consumers in shared memory.
@@ -828,10 +831,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // block-table slice (validated) and, by bulk copy, its queries.
     const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
     bool have_order = false;  // lane 0: the consumers' part-2 order is complete
+    int last_q[kItemSlots];   // lane 0: item number of the last query copy into each slot
+    for (int b = 0; b < kItemSlots; ++b) last_q[b] = -1;
     for (uint32_t it = 0;; ++it) {
       const int slot = it % kItemSlots;
       if (it >= kItemSlots &&
-          !mbar_wait_bounded(smem_addr(qempty + slot), ((it / kItemSlots) - 1) & 1)) {
+          !mbar_wait_bounded(smem_addr(qempty + slot), ((it / kItemSlots) - 1) & 1, p.wait_ns)) {
         if (lane == 0) {
           flag_error(p.err, kErrTimeout);
           *abort_flag = 1;
@@ -844,7 +849,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         item = it == 0 ? static_cast<int>(blockIdx.x)
                        : static_cast<int>(gridDim.x + fetch_ticket(p.counters, p.launch_id));
         if (item >= items1 && item < total_items && !have_order) {
-          have_order = mbar_wait_bounded(smem_addr(sorted), 0);
+          have_order = mbar_wait_bounded(smem_addr(sorted), 0, p.wait_ns);
           if (!have_order) {
             flag_error(p.err, kErrTimeout);
             *abort_flag = 1;
@@ -918,7 +923,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                       static_cast<const uint16_t*>(p.q) +
                           (static_cast<size_t>(seq) * p.num_q_heads + kvh * G) * D,
                       qbytes, ql);
+        last_q[slot] = static_cast<int>(it);
       }
+    }
+    // No query copy may still be landing when the CTA exits. Normally the consumers have waited
+    // for every one; after an abort they may not have. The last copy into a slot completes the
+    // slot's barrier phase of that item, and no later phase was started.
+    if (lane == 0) {
+      for (int b = 0; b < kItemSlots; ++b)
+        if (last_q[b] >= 0)
+          mbar_wait_bounded(smem_addr(qland + b), (static_cast<uint32_t>(last_q[b]) / kItemSlots) & 1,
+                            kDrainLimitNs);
     }
   } else if (warp <= kProducerWarps) {
     // ------------------------------------------------------------------ producer warps
@@ -943,7 +958,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     uint32_t issued_last = 0, any = 0;
     for (uint32_t it = 0;; ++it) {
       const int slot = it % kItemSlots;
-      if (!mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1)) {
+      if (!mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1, p.wait_ns)) {
         ok = false;
         break;
       }
@@ -955,7 +970,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const uint32_t g = g0 + t;
         const int s = static_cast<int>(g % p.stages);
         if (g >= static_cast<uint32_t>(p.stages) &&
-            !mbar_wait_bounded(smem_addr(empty + s), ((g / p.stages) - 1) & 1)) {
+            !mbar_wait_bounded(smem_addr(empty + s), ((g / p.stages) - 1) & 1, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -1015,7 +1030,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         const uint32_t from = issued_last >= span ? issued_last - span + 1 : 0u;
         for (uint32_t g = from; g <= issued_last; ++g)
           if (g % kProducerWarps == static_cast<uint32_t>(pw))
-            mbar_wait_bounded(smem_addr(full + (g % p.stages)), (g / p.stages) & 1);
+            mbar_wait_bounded(smem_addr(full + (g % p.stages)), (g / p.stages) & 1, kDrainLimitNs);
       }
     }
   } else {
@@ -1053,9 +1068,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     uint32_t g0 = 0;
     for (uint32_t it = 0;; ++it) {
       const int slot = it % kItemSlots;
-      bool got = mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1);
+      bool got = mbar_wait_bounded(smem_addr(qfull + slot), (it / kItemSlots) & 1, p.wait_ns);
       const ItemDesc d = items[slot];
-      if (got && d.seq >= 0) got = mbar_wait_bounded(smem_addr(qland + slot), (it / kItemSlots) & 1);
+      if (got && d.seq >= 0)
+        got = mbar_wait_bounded(smem_addr(qland + slot), (it / kItemSlots) & 1, p.wait_ns);
       if (bar_or(kConsumerThreads, !got)) {  // every consumer warp leaves together
         if (ctid == 0) {
           flag_error(p.err, kErrTimeout);
@@ -1074,7 +1090,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int t = cw; t < d.ntiles; t += kConsumerWarps) {
         const uint32_t g = g0 + t;
         const int s = static_cast<int>(g % p.stages);
-        if (!mbar_wait_bounded(smem_addr(full + s), (g / p.stages) & 1)) {
+        if (!mbar_wait_bounded(smem_addr(full + s), (g / p.stages) & 1, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -1134,14 +1150,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (p.max_splits > 1) {
     if (tid == 0) {
       __threadfence();  // this CTA's partials are visible to the whole GPU before it arrives
-      fetch_ticket(p.counters + 2, p.launch_id);
+      if (static_cast<int>(blockIdx.x) != p.stall_cta) fetch_ticket(p.counters + 2, p.launch_id);
       const unsigned long long* ctr = p.counters + 2;
       const unsigned long long start = global_ns();
       bool ok = true;
       for (uint32_t i = 0;; ++i) {
         const unsigned long long v = *reinterpret_cast<const volatile unsigned long long*>(ctr);
         if ((v >> 32) == p.launch_id && static_cast<uint32_t>(v) >= gridDim.x) break;
-        if ((i & 63u) == 63u && global_ns() - start > kWaitLimitNs) {
+        if ((i & 63u) == 63u && global_ns() - start > p.wait_ns) {
           ok = false;
           break;
         }

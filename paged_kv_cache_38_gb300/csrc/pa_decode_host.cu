@@ -332,6 +332,8 @@ pa_status run_decode(const pa_decode_args& a, cudaStream_t stream, std::string& 
   p.score_scale = a.scale * a.k_scale * kLog2e;
   p.v_scale = a.v_scale;
   p.q_bf16 = a.q_dtype == PA_BF16 ? 1 : 0;
+  p.wait_ns = launch_wait_ns();
+  p.stall_cta = launch_stall_cta();
 
   const int group = a.num_q_heads / a.num_kv_heads;
   const int elt_q = 2;

@@ -16,8 +16,11 @@ constexpr int kErrBlockId = 1;
 constexpr int kErrCtxLen = 2;
 constexpr int kErrTimeout = 4;
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer.
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// A wait on another warp, role or CTA gives up after the launch's wait limit (one second of
+// %globaltimer unless the host shortened it: pa_testing_set_wait_limit).
+// A wait for this thread's own copies or MMAs to complete (before its CTA may exit) always uses
+// this limit: they complete by themselves, so a shortened limit must not cut the wait short.
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 
 __device__ __forceinline__ void flag_error(int32_t* err, int bits) {
   if (err != nullptr) atomicOr(err, bits);
@@ -80,14 +83,15 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most kWaitLimitNs.
+// Wait for the phase with the given parity to complete, for at most limit_ns.
 // Returns false on timeout (the caller records kErrTimeout and winds down).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long start = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - start > kWaitLimitNs) return false;
+    if ((i & 255u) == 0 && global_ns() - start > limit_ns) return false;
   }
 }
 

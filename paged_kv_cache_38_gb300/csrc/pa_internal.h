@@ -71,6 +71,15 @@ pa_status run_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t nu
                           size_t block_bytes, pa_swap_dir dir, void* staging, size_t staging_bytes,
                           cudaStream_t stream, std::string& msg);
 
+// A scheduler plan's moves: swap-outs ((GPU block, CPU slot) pairs), swap-ins ((CPU slot, GPU
+// block) pairs), copy-on-write (src, dst) pairs, all in host memory, into launches in that order.
+pa_status run_plan_moves(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                         int32_t num_blocks, size_t block_bytes, void* cpu_pool,
+                         int32_t num_cpu_blocks, const int32_t* swap_out, int32_t num_swap_out,
+                         const int32_t* swap_in, int32_t num_swap_in, const int32_t* copies,
+                         int32_t num_copies, int32_t* err_flag, cudaStream_t stream,
+                         std::string& msg);
+
 // Records msg as the calling thread's last-error message and returns st.
 pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string& msg);
 pa_status encode_pool_rows_map(CUtensorMap* map, const void* pool, long long rows, int head_dim,
@@ -78,6 +87,10 @@ pa_status encode_pool_rows_map(CUtensorMap* map, const void* pool, long long row
 pa_status encode_query_tile_map(CUtensorMap* map, const void* q, int num_tokens, int num_q_heads,
                                 int head_dim, int group, int tokens, std::string& msg);
 pa_status record_error(pa_status st, const std::string& msg);
+
+// Wait limit (ns) and stalled CTA (-1: none) for the next launches; see pa_testing_set_wait_limit.
+unsigned long long launch_wait_ns();
+int launch_stall_cta();
 
 // Sets msg from a CUDA error and returns PA_ECUDA (or PA_OK for cudaSuccess).
 pa_status cuda_status(cudaError_t e, const char* what, std::string& msg);

@@ -190,15 +190,19 @@ __global__ void __launch_bounds__(256) pa_write_kv_fp8_kernel(const __grid_const
 
 // ------------------------------------------------------------------ region copies
 
-enum CopyMode { kCopyPairs = 0, kPoolToBuf = 1, kBufToPool = 2 };
+// kCopyPairs: device (src, dst) pairs. kPoolToBuf / kBufToPool: entry i is block ids[i] and
+// buffer slot i. kHostPairs: (src, dst) pairs in ids. kPoolToSlots: (block, buffer slot) pairs in
+// ids; kSlotsToPool: (buffer slot, block) pairs in ids (a plan's swap lists).
+enum CopyMode { kCopyPairs = 0, kPoolToBuf = 1, kBufToPool = 2, kHostPairs = 3, kPoolToSlots = 4,
+                kSlotsToPool = 5 };
 
 struct CopyParams {
   uint8_t* k[kMaxLayers];
   uint8_t* v[kMaxLayers];
-  uint8_t* buf;          // host-mapped pinned buffer or device staging, [n][layers][2][bytes]
+  uint8_t* buf;          // host-mapped pinned buffer or device staging, [slots][layers][2][bytes]
   const int32_t* pairs;  // kCopyPairs: device [n][2]
   int32_t* err;
-  int32_t ids[kMaxIdsPerLaunch];  // kPoolToBuf / kBufToPool: block ids of this launch
+  int32_t ids[kMaxIdsPerLaunch];  // block ids, or id pairs, of this launch (host-validated)
   long long block_bytes;
   int mode, n, num_layers, num_blocks, slices_per_region;
 };
@@ -217,8 +221,15 @@ __global__ void __launch_bounds__(kCopyThreads) pa_copy_regions_kernel(const __g
     const uint8_t* src;
     uint8_t* dst;
     uint8_t* pool = kv ? p.v[l] : p.k[l];
-    if (p.mode == kCopyPairs) {
-      const int s = __ldg(p.pairs + 2 * i), d = __ldg(p.pairs + 2 * i + 1);
+    if (p.mode == kCopyPairs || p.mode == kHostPairs) {
+      int s, d;
+      if (p.mode == kCopyPairs) {
+        s = __ldg(p.pairs + 2 * i);
+        d = __ldg(p.pairs + 2 * i + 1);
+      } else {
+        s = p.ids[2 * i];
+        d = p.ids[2 * i + 1];
+      }
       if (s < 0 || s >= p.num_blocks || d < 0 || d >= p.num_blocks) {
         if (threadIdx.x == 0 && slice == 0 && l == 0 && kv == 0) flag_error(p.err, kErrBlockId);
         continue;
@@ -226,10 +237,19 @@ __global__ void __launch_bounds__(kCopyThreads) pa_copy_regions_kernel(const __g
       src = pool + s * p.block_bytes;
       dst = pool + d * p.block_bytes;
     } else {
-      uint8_t* slab = pool + static_cast<long long>(p.ids[i]) * p.block_bytes;
-      uint8_t* packed = p.buf + r * p.block_bytes;
-      src = p.mode == kPoolToBuf ? slab : packed;
-      dst = p.mode == kPoolToBuf ? packed : slab;
+      long long blk = p.ids[i], slot = i;
+      if (p.mode == kPoolToSlots) {
+        blk = p.ids[2 * i];
+        slot = p.ids[2 * i + 1];
+      } else if (p.mode == kSlotsToPool) {
+        slot = p.ids[2 * i];
+        blk = p.ids[2 * i + 1];
+      }
+      uint8_t* slab = pool + blk * p.block_bytes;
+      uint8_t* packed = p.buf + ((slot * p.num_layers + l) * 2 + kv) * p.block_bytes;
+      const bool out = p.mode == kPoolToBuf || p.mode == kPoolToSlots;
+      src = out ? slab : packed;
+      dst = out ? packed : slab;
     }
     const long long off0 = static_cast<long long>(slice) * kSliceBytes;
     const uint4* s4 = reinterpret_cast<const uint4*>(src + off0);
@@ -529,6 +549,92 @@ pa_status run_swap_blocks(void* const* k_pools, void* const* v_pools, int32_t nu
     st = cuda_status(cudaMemcpyAsync(host_buf, staging, total, cudaMemcpyDeviceToHost, stream),
                      "pa_swap_blocks device-to-host copy", msg);
   }
+  return st;
+}
+
+pa_status run_plan_moves(void* const* k_pools, void* const* v_pools, int32_t num_layers,
+                         int32_t num_blocks, size_t block_bytes, void* cpu_pool,
+                         int32_t num_cpu_blocks, const int32_t* swap_out, int32_t num_swap_out,
+                         const int32_t* swap_in, int32_t num_swap_in, const int32_t* copies,
+                         int32_t num_copies, int32_t* err_flag, cudaStream_t stream,
+                         std::string& msg) {
+  pa_status st = check_pools(k_pools, v_pools, num_layers, block_bytes, num_blocks, msg);
+  if (st != PA_OK) return st;
+  if (num_swap_out < 0 || num_swap_in < 0 || num_copies < 0 || num_cpu_blocks < 0) {
+    msg = "move counts and num_cpu_blocks must be >= 0";
+    return PA_EINVAL;
+  }
+  if ((num_swap_out && !swap_out) || (num_swap_in && !swap_in) || (num_copies && !copies)) {
+    msg = "a non-empty move list is NULL";
+    return PA_EINVAL;
+  }
+  // every id is known on the host: check them all before anything is enqueued
+  auto check = [&](const int32_t* pairs, int n, int col_slot, const char* what) -> bool {
+    for (int i = 0; i < n; ++i) {
+      for (int c = 0; c < 2; ++c) {
+        const int32_t v = pairs[2 * i + c];
+        const int32_t limit = c == col_slot ? num_cpu_blocks : num_blocks;
+        if (v < 0 || v >= limit) {
+          msg = std::string(what) + "[" + std::to_string(i) + "][" + std::to_string(c) +
+                "] = " + std::to_string(v) + " is outside " +
+                (c == col_slot ? "the CPU pool" : "the GPU pool");
+          return false;
+        }
+      }
+    }
+    return true;
+  };
+  if (!check(swap_out, num_swap_out, 1, "swap_out") || !check(swap_in, num_swap_in, 0, "swap_in") ||
+      !check(copies, num_copies, -1, "copies"))
+    return PA_EINVAL;
+  uint8_t* mapped = nullptr;
+  if (num_swap_out + num_swap_in > 0) {
+    if (!cpu_pool || !aligned16(cpu_pool)) {
+      msg = "cpu_pool (16-byte aligned pinned memory) is required for swaps";
+      return PA_EINVAL;
+    }
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, cpu_pool) != cudaSuccess) {
+      cudaGetLastError();
+      msg = "cpu_pool is not known to CUDA";
+      return PA_EINVAL;
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) {
+      msg = "cpu_pool must be pinned host memory (cudaHostAlloc / cudaHostRegister)";
+      return PA_EINVAL;
+    }
+    mapped = static_cast<uint8_t*>(attr.devicePointer);
+  }
+  CopyParams* p = new CopyParams();
+  fill_pools(*p, k_pools, v_pools, num_layers);
+  p->buf = mapped;
+  p->err = err_flag;
+  p->block_bytes = static_cast<long long>(block_bytes);
+  p->num_layers = num_layers;
+  p->num_blocks = num_blocks;
+  p->slices_per_region = static_cast<int>((block_bytes + kSliceBytes - 1) / kSliceBytes);
+  // swap-outs, then swap-ins, then copy-on-write copies, in stream order
+  const struct {
+    const int32_t* pairs;
+    int n;
+    int mode;
+    const char* what;
+  } lists[3] = {{swap_out, num_swap_out, kPoolToSlots, "swap-out"},
+                {swap_in, num_swap_in, kSlotsToPool, "swap-in"},
+                {copies, num_copies, kHostPairs, "copy-on-write"}};
+  constexpr int kPairsPerLaunch = kMaxIdsPerLaunch / 2;
+  for (const auto& m : lists) {
+    for (int i0 = 0; i0 < m.n && st == PA_OK; i0 += kPairsPerLaunch) {
+      const int cnt = std::min(kPairsPerLaunch, m.n - i0);
+      std::memcpy(p->ids, m.pairs + 2 * i0, sizeof(int32_t) * 2 * cnt);
+      p->mode = m.mode;
+      p->n = cnt;
+      const long long units = static_cast<long long>(cnt) * num_layers * 2 * p->slices_per_region;
+      pa_copy_regions_kernel<<<copy_grid(units), kCopyThreads, 0, stream>>>(*p);
+      st = cuda_status(cudaGetLastError(), m.what, msg);
+    }
+  }
+  delete p;
   return st;
 }
 

@@ -20,10 +20,40 @@ static __device__ __align__(256) unsigned char g_static_scratch[PA_STATIC_WORKSP
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
+// Per device: the array's device address and the context it was looked up in. After a device
+// reset (a new primary context) the module is loaded again and the array may sit elsewhere, so
+// the address is looked up again whenever the current context differs.
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of g_static_scratch on the current device, looked up once per device. In host
-// code the array's name only stands for the symbol, so the address must come from the runtime.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+pa_status current_context(CUcontext* ctx, std::string& msg) {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+  });
+  if (fn == nullptr) {
+    msg = "cuCtxGetCurrent is not available from the driver";
+    return PA_ECUDA;
+  }
+  *ctx = nullptr;
+  if (fn(ctx) != CUDA_SUCCESS) {
+    msg = "cuCtxGetCurrent failed";
+    return PA_ECUDA;
+  }
+  return PA_OK;  // *ctx stays NULL while the thread has no current context yet
+}
+
+// Device address of g_static_scratch on the current device, looked up once per device and
+// context. In host code the array's name only stands for the symbol, so the address must come
+// from the runtime.
 pa_status scratch_address(void** out, std::string& msg) {
   int dev = 0;
   pa_status st = cuda_status(cudaGetDevice(&dev), "cudaGetDevice", msg);
@@ -32,13 +62,20 @@ pa_status scratch_address(void** out, std::string& msg) {
     msg = "device ordinal beyond the static scratch table";
     return PA_EUNSUPPORTED;
   }
+  CUcontext ctx = nullptr;
+  st = current_context(&ctx, msg);
+  if (st != PA_OK) return st;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || ctx == nullptr || g_scratch_ctx[dev] != ctx) {
     void* ptr = nullptr;
+    // (makes the device's primary context current first if the thread had none)
     st = cuda_status(cudaGetSymbolAddress(&ptr, g_static_scratch),
                      "cudaGetSymbolAddress of the static decode scratch", msg);
     if (st != PA_OK) return st;
+    st = current_context(&ctx, msg);
+    if (st != PA_OK) return st;
     g_scratch_ptr[dev] = ptr;
+    g_scratch_ctx[dev] = ctx;
   }
   *out = g_scratch_ptr[dev];
   return PA_OK;

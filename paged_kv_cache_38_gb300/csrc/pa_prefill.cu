@@ -104,6 +104,8 @@ struct PrefillParams {
   int pairs;         // num_seqs * num_kv_heads
   int total;         // pairs * tiles rounded up to whole blocks
   float scale_log2;  // scale * log2(e)
+  unsigned long long wait_ns;  // limit of a wait on another role (1 s unless a test shortened it)
+  int stall_cta;     // testing: this CTA's MMA issuer stops after its first S group (-1: none)
 };
 
 // A published work item; s < 0 ends the work.
@@ -252,7 +254,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           break;
         }
         const int slot = k % kSlots;
-        if (k >= kSlots && !mbar_wait_bounded(smem_addr(item_empty + slot), ((k / kSlots) - 1) & 1)) {
+        if (k >= kSlots &&
+            !mbar_wait_bounded(smem_addr(item_empty + slot), ((k / kSlots) - 1) & 1, p.wait_ns)) {
           fail();
           it.s = -1;
         }
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         mbar_arrive(smem_addr(item_full + slot));
         if (it.s < 0) break;
         // the query buffer is free once the previous item's last S MMA has completed
-        if (k >= 1 && !mbar_wait_bounded(smem_addr(q_empty), (k - 1) & 1)) {
+        if (k >= 1 && !mbar_wait_bounded(smem_addr(q_empty), (k - 1) & 1, p.wait_ns)) {
           fail();
           break;
         }
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         ++k;
       }
       // no query copy may still be landing when the CTA exits (matters after an abort)
-      if (k >= 1) mbar_wait_bounded(smem_addr(q_full), (k - 1) & 1);
+      if (k >= 1) mbar_wait_bounded(smem_addr(q_full), (k - 1) & 1, kDrainLimitNs);
     }
   } else if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ K/V producers
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int slot = k % kSlots;
-        if (!mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1)) {
+        if (!mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1, p.wait_ns)) {
           fail();
           break;
         }
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         for (int j = 0; j < it.ntiles; ++j, ++J) {
           const int st = J % kPfStages;
           if (J >= kPfStages &&
-              !mbar_wait_bounded(smem_addr(emptyb + st), ((J / kPfStages) - 1) & 1)) {
+              !mbar_wait_bounded(smem_addr(emptyb + st), ((J / kPfStages) - 1) & 1, p.wait_ns)) {
             fail();
             ok = false;
             break;
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       }
       // no copy of this CTA may still be landing when it exits (matters after an abort)
       for (int jj = max(0, J - kPfStages); jj < J; ++jj)
-        mbar_wait_bounded(smem_addr(fullb + jj % kPfStages), (jj / kPfStages) & 1);
+        mbar_wait_bounded(smem_addr(fullb + jj % kPfStages), (jj / kPfStages) & 1, kDrainLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -381,6 +384,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       PfItem iP{};
       int nO = 0;  // items whose O is complete
       bool ok = true;
+      const bool stalled = static_cast<int>(blockIdx.x) == p.stall_cta;
       uint32_t idle = 0;
       unsigned long long idle_since = 0;
       for (;;) {
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             break;  // every item is done
           }
         }
-        if (haveP && npv < ns) {
+        if (haveP && npv < ns && !stalled) {
           const int stp = npv % kPfStages;
           if (mbar_test(smem_addr(p_full), npv & 1) &&
               mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1) &&
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           }
           did = true;
         }
-        if (haveS) {
+        if (haveS && !(stalled && ns >= 1)) {
           const int st = ns % kPfStages, b = ns & 1;
           if (mbar_test(smem_addr(k_full + st), (ns / kPfStages) & 1) &&
               (ns < 2 || mbar_test(smem_addr(s_free + b), ((ns >> 1) - 1) & 1)) &&
@@ -460,7 +464,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           idle = 0;
         } else if (idle++ == 0) {
           idle_since = global_ns();
-        } else if ((idle & 63u) == 0 && global_ns() - idle_since > kWaitLimitNs) {
+        } else if ((idle & 63u) == 0 && global_ns() - idle_since > p.wait_ns) {
           ok = false;
           break;
         }
@@ -468,7 +472,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       if (!ok) fail();
       // every MMA this thread issued has completed before tensor memory is released
       umma_commit(smem_addr(drain));
-      mbar_wait_bounded(smem_addr(drain), 0);
+      mbar_wait_bounded(smem_addr(drain), 0, kDrainLimitNs);
     }
   } else if (warp >= kSoftmaxWarp0) {
     // ------------------------------------------------------------------ softmax warpgroup
@@ -517,7 +521,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     };
     for (int k = 0;; ++k) {
       const int slot = k % kSlots;
-      ok = mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1);
+      ok = mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1, p.wait_ns);
       if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
         ok = false;
         break;
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.ntiles; ++j, ++jx) {
         const int b = jx & 1;
-        ok = mbar_wait_bounded(smem_addr(s_full + b), (jx >> 1) & 1);
+        ok = mbar_wait_bounded(smem_addr(s_full + b), (jx >> 1) & 1, p.wait_ns);
         if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
           ok = false;
           break;
@@ -616,7 +620,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         m = m_new;
 
         if (jx >= 1) {  // PV of the previous tile done: O is stable and the P buffer free
-          ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1);
+          ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1, p.wait_ns);
           if (__any_sync(0xffffffffu, !ok)) {
             ok = false;
             break;
@@ -626,7 +630,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         if (j == it.ntiles - 1 && key0 + kPfKeys > it.L) {
           // value rows past the cache's last position (stale slots, or not loaded) become zero,
           // so that zero weights cannot meet a NaN; the tile's V copies must have landed first
-          ok = mbar_wait_bounded(smem_addr(v_full + (jx % kPfStages)), (jx / kPfStages) & 1);
+          ok = mbar_wait_bounded(smem_addr(v_full + (jx % kPfStages)), (jx / kPfStages) & 1,
+                                 p.wait_ns);
           if (__any_sync(0xffffffffu, !ok)) {
             ok = false;
             break;
@@ -672,7 +677,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       pend_slot = slot;
     }
     if (ok && pend) {  // the last item's epilogue, once its last PV has completed
-      ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1);
+      ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1, p.wait_ns);
       if (__any_sync(0xffffffffu, !ok)) ok = false;
       if (ok) {
         tc_fence_after();
@@ -823,6 +828,8 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   p.pairs = a.num_seqs * a.num_kv_heads;
   p.total = static_cast<int>(total);
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.wait_ns = launch_wait_ns();
+  p.stall_cta = launch_stall_cta();
 
   const int D = a.head_dim;
   const size_t regions = static_cast<size_t>(D / 64);

@@ -1,7 +1,8 @@
 // pa_scheduler.cpp - host scheduler and KV block manager (include/pa_scheduler.h).
 //
 // Plans the block tables, slots, copy-on-write pairs and swaps of each decode step; the
-// policy and its sources are stated in the header. Plain host C++: no CUDA call.
+// policy and its sources are stated in the header. Plain host C++; only the last entry point,
+// which enqueues a plan's block moves, reaches the mover kernels (pa_movers.cu).
 #include <algorithm>
 #include <deque>
 #include <memory>
@@ -375,6 +376,19 @@ int32_t pa_scheduler_free_blocks(const pa_scheduler* s, int32_t* out, int32_t ca
 
 int32_t pa_scheduler_has_unfinished(const pa_scheduler* s) {
   return s != nullptr && (!s->waiting.empty() || !s->running.empty()) ? 1 : 0;
+}
+
+pa_status pa_scheduler_execute_moves(const pa_step_plan* plan, void* const* k_pools,
+                                     void* const* v_pools, int32_t num_layers, int32_t num_blocks,
+                                     size_t block_bytes, void* cpu_pool, int32_t num_cpu_blocks,
+                                     int32_t* err_flag, pa_stream stream) {
+  if (plan == nullptr) return pa::record_error(PA_EINVAL, "plan is NULL");
+  std::string msg;
+  const pa_status st = pa::run_plan_moves(
+      k_pools, v_pools, num_layers, num_blocks, block_bytes, cpu_pool, num_cpu_blocks,
+      plan->swap_out, plan->num_swap_out, plan->swap_in, plan->num_swap_in, plan->copies,
+      plan->num_copies, err_flag, reinterpret_cast<cudaStream_t>(stream), msg);
+  return st == PA_OK ? PA_OK : pa::record_error(st, msg);
 }
 
 }  // extern "C"

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
                                      ctypes.c_int, _vp, ctypes.c_size_t, _vp]
         L.pa_decode_static_workspace.restype = ctypes.c_int
         L.pa_decode_static_workspace.argtypes = [ctypes.POINTER(pa_decode_args), _vp]
+        L.pa_testing_set_wait_limit.restype = ctypes.c_int
+        L.pa_testing_set_wait_limit.argtypes = [ctypes.c_uint64, _i32]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_status_string.argtypes = [ctypes.c_int]
         L.pa_last_error_message.restype = ctypes.c_char_p
@@ -293,3 +295,9 @@ def pa_swap_blocks(k_pools: Sequence[torch.Tensor], v_pools: Sequence[torch.Tens
     _check(lib().pa_swap_blocks(kp, vp, len(k_pools), _ptr(host_buf), ids.data_ptr(), ids.numel(),
                                 p0.shape[0], block_bytes, direction, _ptr(staging), st_bytes,
                                 _stream(stream)))
+
+
+def pa_testing_set_wait_limit(wait_ns: int, stall_cta: int = -1) -> None:
+    """Shorten the kernels' waits on one another (0 restores one second) and, with stall_cta
+    >= 0, make that CTA withhold its part so the others' waits run out. For tests only."""
+    _check(lib().pa_testing_set_wait_limit(int(wait_ns), int(stall_cta)))

@@ -46,6 +46,11 @@ def _bind(L) -> None:
     L.pa_scheduler_free_blocks.argtypes = [ctypes.c_void_p, _i32p, ctypes.c_int32]
     L.pa_scheduler_has_unfinished.restype = ctypes.c_int32
     L.pa_scheduler_has_unfinished.argtypes = [ctypes.c_void_p]
+    L.pa_scheduler_execute_moves.restype = ctypes.c_int
+    L.pa_scheduler_execute_moves.argtypes = [ctypes.POINTER(pa_step_plan), ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int32,
+                                             ctypes.c_void_p, ctypes.c_void_p]
     L._scheduler_bound = True
 
 
@@ -163,29 +168,27 @@ class Scheduler:
 
 
 def execute_moves(plan: Plan, k_pools, v_pools, cpu_pool, *, err_flag=None, stream=None) -> None:
-    """Enqueue a plan's block moves in the order the plan requires: swap-outs (GPU block ->
-    CPU slot), swap-ins (CPU slot -> GPU block), then copy-on-write copies. ``cpu_pool`` is a
-    pinned uint8 tensor [num_cpu_blocks][layers][2][block_bytes]; runs of consecutive CPU slots
-    move in one call. The KV writes and the decode are the caller's (they need the new K/V)."""
-    import torch
+    """pa_scheduler_execute_moves on a plan's move lists: swap-outs (GPU block -> CPU slot),
+    swap-ins (CPU slot -> GPU block), then copy-on-write copies, enqueued by the library in that
+    order. ``cpu_pool`` is a pinned uint8 tensor [num_cpu_blocks][layers][2][block_bytes] (or
+    None when the plan has no swaps). The KV writes and the decode are the caller's (they need
+    the new K/V)."""
+    from .pa import _check, _ptr, _ptr_array, _stream
 
-    from .pa import PA_SWAP_IN, PA_SWAP_OUT, pa_copy_blocks, pa_swap_blocks
-
-    def runs(pairs, slot_col):
-        i = 0
-        while i < len(pairs):
-            j = i + 1
-            while j < len(pairs) and pairs[j][slot_col] == pairs[j - 1][slot_col] + 1:
-                j += 1
-            yield pairs[i][slot_col], [p[1 - slot_col] for p in pairs[i:j]]
-            i = j
-
-    for c0, blocks in runs(plan.swap_out, 1) if len(plan.swap_out_np) else ():
-        pa_swap_blocks(k_pools, v_pools, cpu_pool[c0:c0 + len(blocks)], blocks, PA_SWAP_OUT,
-                       stream=stream)
-    for c0, blocks in runs(plan.swap_in, 0) if len(plan.swap_in_np) else ():
-        pa_swap_blocks(k_pools, v_pools, cpu_pool[c0:c0 + len(blocks)], blocks, PA_SWAP_IN,
-                       stream=stream)
-    if len(plan.copies_np):
-        pairs = torch.from_numpy(plan.copies_np).to(k_pools[0].device, non_blocking=False)
-        pa_copy_blocks(k_pools, v_pools, pairs, err_flag=err_flag, stream=stream)
+    L = lib()
+    _bind(L)
+    p = pa_step_plan()
+    lists = {}
+    for name, arr in (("copies", plan.copies_np), ("swap_out", plan.swap_out_np),
+                      ("swap_in", plan.swap_in_np)):
+        a = np.ascontiguousarray(arr, dtype=np.int32)
+        lists[name] = a  # kept alive for the call
+        setattr(p, "num_" + name, a.shape[0] if a.size else 0)
+        setattr(p, name, a.ctypes.data_as(_i32p) if a.size else None)
+    k0 = k_pools[0]
+    block_bytes = k0[0].numel() * k0.element_size()
+    ncpu = 0 if cpu_pool is None else cpu_pool.shape[0]
+    _check(L.pa_scheduler_execute_moves(ctypes.byref(p), _ptr_array(k_pools),
+                                        _ptr_array(v_pools), len(k_pools), k0.shape[0],
+                                        block_bytes, _ptr(cpu_pool), ncpu, _ptr(err_flag),
+                                        _stream(stream)))

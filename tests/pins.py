@@ -360,15 +360,19 @@ def _prefill_specs():
         S["gqa_pressure"].scaled(num_seqs=5, ctx_range=(20, 90), shared_prompt=32),
         synth.DecodeSpec("g2_b8", 3, 8, 4, 64, 8, "bf16", "bf16", ctx_range=(1, 40)),
         synth.DecodeSpec("g16_b32", 2, 16, 1, 128, 32, "f16", "f16", ctx_range=(30, 70)),
+        # an FP8 cache (bf16 queries, E4M3 K/V with per-tensor scales), as a recomputed
+        # request of the FP8 workload is prefilled
+        S["fp8_long"].scaled(num_seqs=4, ctx_range=(15, 80)),
     ]
 
 
 def _run_prefill(orc, case, qs, q):
     spec = case.spec
     return orc.prefill(q, case.k_pool, case.v_pool, case.block_tables, case.ctx_lens, qs,
-                       dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
+                       dtype=spec.kv_dtype, q_dtype=spec.q_dtype, num_q_heads=spec.num_q_heads,
                        num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
-                       block_size=spec.block_size, scale=case.scale)
+                       block_size=spec.block_size, scale=case.scale, k_scale=case.k_scale,
+                       v_scale=case.v_scale)
 
 
 def pin_prefill_equals_library_attention(orc):

@@ -27,11 +27,12 @@ def declared_functions(header=None):
 def test_header_declares_the_boundary():
     assert declared_functions(HEADER) == sorted([
         "pa_copy_blocks", "pa_decode", "pa_decode_static_workspace", "pa_decode_workspace_size",
-        "pa_last_error_message", "pa_prefill", "pa_status_string", "pa_swap_blocks", "pa_write_kv",
-        "pa_write_kv_fp8"])
+        "pa_last_error_message", "pa_prefill", "pa_status_string", "pa_swap_blocks",
+        "pa_testing_set_wait_limit", "pa_write_kv", "pa_write_kv_fp8"])
     assert declared_functions(os.path.join(os.path.dirname(HEADER), "pa_scheduler.h")) == sorted([
         "pa_scheduler_add_request", "pa_scheduler_create", "pa_scheduler_destroy",
-        "pa_scheduler_free_blocks", "pa_scheduler_has_unfinished", "pa_scheduler_step"])
+        "pa_scheduler_execute_moves", "pa_scheduler_free_blocks", "pa_scheduler_has_unfinished",
+        "pa_scheduler_step"])
 
 
 def test_library_exports_every_declared_symbol():
@@ -110,3 +111,32 @@ def test_workspace_size_and_validation_on_host():
     ids = (ctypes.c_int32 * 1)(20)
     assert lib.pa_swap_blocks(arr, arr, 1, None, ids, 1, 10, 4096, pa.PA_SWAP_OUT, None, 0,
                               None) == pa.PA_EINVAL
+
+
+def test_wait_limit_hook_validates_on_the_host():
+    """The testing hook of the bounded waits: a CTA index below -1 is refused; a valid setting
+    and the reset to the default are accepted (nothing is launched)."""
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_testing_set_wait_limit(1000, -2)
+    assert e.value.status == pa.PA_EINVAL
+    pa.pa_testing_set_wait_limit(1000, 3)
+    pa.pa_testing_set_wait_limit(0, -1)
+
+
+def test_execute_moves_validates_ids_on_the_host():
+    """pa_scheduler_execute_moves checks every block id and CPU slot of the plan before it
+    enqueues anything (the pool pointers are never dereferenced on this path)."""
+    from paged_kv_cache_38_gb300 import scheduler as sch
+
+    L = pa.lib()
+    sch._bind(L)
+    fake = (ctypes.c_void_p * 1)(1 << 20)
+    for field, pairs in (("copies", [3, 64]), ("swap_out", [2, 8]), ("swap_in", [-1, 0])):
+        plan = sch.pa_step_plan()
+        arr = (ctypes.c_int32 * 2)(*pairs)
+        setattr(plan, "num_" + field, 1)
+        setattr(plan, field, ctypes.cast(arr, sch._i32p))
+        st = L.pa_scheduler_execute_moves(ctypes.byref(plan), fake, fake, 1, 64, 4096, None, 8,
+                                          None, None)
+        assert st == pa.PA_EINVAL, field
+        assert b"outside" in L.pa_last_error_message(), field

@@ -265,17 +265,19 @@ def test_swap_round_trip(staged):
     exp = np.zeros(n * L * 2 * bb, np.uint8)
     assert oracle.load().swap_blocks(kps, vps, exp, out_ids, block_bytes=bb, direction="out") == 0
     assert np.array_equal(host.numpy(), exp)
-    # the released blocks are reused by someone else, then the victim comes back elsewhere
+    # the released blocks are reused by someone else (the same bytes land in the GPU pools and
+    # in the oracle's copies), then the victim comes back elsewhere
     for p in case.k_pools + case.v_pools:
         p.view(torch.uint8).view(case.num_blocks, -1)[torch.from_numpy(out_ids).long().cuda()] = 0x7F
+    for p in kps + vps:
+        p.reshape(case.num_blocks, -1)[out_ids] = 0x7F
     pa.pa_swap_blocks(case.k_pools, case.v_pools, host, in_ids, pa.PA_SWAP_IN, staging=staging)
     torch.cuda.synchronize()
     assert oracle.load().swap_blocks(kps, vps, exp, in_ids, block_bytes=bb, direction="in") == 0
+    # whole pools, every layer: the restored blocks and every block the swap-in must not touch
     for l in range(L):
-        np.testing.assert_array_equal(_u8(case.k_pools[l]).reshape(case.num_blocks, -1)[in_ids],
-                                      kps[l].reshape(case.num_blocks, -1)[in_ids])
-        np.testing.assert_array_equal(_u8(case.v_pools[l]).reshape(case.num_blocks, -1)[in_ids],
-                                      vps[l].reshape(case.num_blocks, -1)[in_ids])
+        np.testing.assert_array_equal(_u8(case.k_pools[l]), kps[l])
+        np.testing.assert_array_equal(_u8(case.v_pools[l]), vps[l])
     bt = case.block_tables.clone()
     bt[victim, :n] = torch.from_numpy(in_ids).cuda()
     after = gpu_decode(case, block_tables=bt)
@@ -294,3 +296,45 @@ def test_swap_rejects_pageable_and_bad_ids():
     with pytest.raises(pa.PaError) as e:
         pa.pa_swap_blocks([case.k_pool], [case.v_pool], pinned, [0, 9], pa.PA_SWAP_OUT)
     assert e.value.status == pa.PA_EINVAL
+
+
+def test_execute_moves_matches_oracle_on_whole_pools():
+    """pa_scheduler_execute_moves on a plan with scattered CPU slots: swap-outs, then swap-ins,
+    then copy-on-write copies, over 3 layers. The GPU pools and the pinned CPU pool equal the
+    oracle's (the same moves applied one pair at a time by its literal swap and copy formulas)
+    byte for byte, untouched blocks and slots included."""
+    from paged_kv_cache_38_gb300 import scheduler as sch
+
+    orc = oracle.load()
+    rng = np.random.default_rng(90)
+    L, nblk, ncpu, bb = 3, 48, 20, 8 * 1024
+    kps = [rng.integers(0, 256, nblk * bb, dtype=np.uint8) for _ in range(L)]
+    vps = [rng.integers(0, 256, nblk * bb, dtype=np.uint8) for _ in range(L)]
+    cpu = rng.integers(0, 256, ncpu * L * 2 * bb, dtype=np.uint8)
+    perm = rng.permutation(nblk)
+    slots = rng.permutation(ncpu)
+    swap_out = np.stack([perm[:5], slots[:5]], 1).astype(np.int32)       # (block, slot)
+    swap_in = np.stack([slots[5:9], perm[5:9]], 1).astype(np.int32)      # (slot, block)
+    copies = np.stack([perm[9:12], perm[12:15]], 1).astype(np.int32)     # (src, dst)
+    gk = [torch.from_numpy(p.copy()).cuda().view(nblk, -1) for p in kps]
+    gv = [torch.from_numpy(p.copy()).cuda().view(nblk, -1) for p in vps]
+    gcpu = torch.from_numpy(cpu.copy()).view(ncpu, L, 2, bb).pin_memory()
+    plan = sch.Plan(*([np.zeros(0, np.int64)] + [np.zeros((0, 1), np.int32)]
+                      + [np.zeros(0, np.int32)] * 3 + [np.zeros(0, np.int64)]
+                      + [copies, swap_out, swap_in, [], [], 0]))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sch.execute_moves(plan, gk, gv, gcpu, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    per_slot = L * 2 * bb
+    for b, c in swap_out:
+        view = cpu[c * per_slot:(c + 1) * per_slot]
+        assert orc.swap_blocks(kps, vps, view, [b], block_bytes=bb, direction="out") == 0
+    for c, b in swap_in:
+        view = cpu[c * per_slot:(c + 1) * per_slot]
+        assert orc.swap_blocks(kps, vps, view, [b], block_bytes=bb, direction="in") == 0
+    assert orc.copy_blocks(kps, vps, copies, block_bytes=bb) == 0
+    for l in range(L):
+        assert np.array_equal(gk[l].cpu().numpy().reshape(-1), kps[l])
+        assert np.array_equal(gv[l].cpu().numpy().reshape(-1), vps[l])
+    assert np.array_equal(gcpu.numpy().reshape(-1), cpu)

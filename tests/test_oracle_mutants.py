@@ -23,7 +23,7 @@ MUTANTS = [
     ('no_normalisation', 'o[d] = acc / denom;', 'o[d] = acc;', 2),
     ('k_scale_dropped', 'element(k_pool, first + d, kv_dtype) * k_scale', 'element(k_pool, first + d, kv_dtype)', 1),
     ('v_scale_dropped', 'element(v_pool, first + d, kv_dtype) * v_scale', 'element(v_pool, first + d, kv_dtype)', 1),
-    ('v_read_from_k_pool', 'element(v_pool, first + d, kv_dtype)', 'element(k_pool, first + d, kv_dtype)', 1),
+    ('v_read_from_k_pool', 'element(v_pool, first + d, kv_dtype)', 'element(k_pool, first + d, kv_dtype)', 2),
     ('drops_newest_token', 'for (int t = 0; t < L; ++t) {\n        double dot', 'for (int t = 0; t < L - 1; ++t) {\n        double dot', 1),
     ('e4m3_bias_8', 'e - 7 - 3', 'e - 8 - 3', 1),
     ('e4m3_subnormal_as_normal', 'mag = ldexp((double)f, -6 - 3);', 'mag = ldexp((double)(8 + f), -7 - 3);', 1),
@@ -50,7 +50,11 @@ MUTANTS = [
     ('prefill_position_from_chunk_start', 'const int last = L - n + i;', 'const int last = i;', 1),
     ('prefill_excludes_itself', 'const int last = L - n + i;', 'const int last = L - n + i - 1;', 1),
     ('prefill_scale_dropped', '          score[t] = scale * dot;', '          score[t] = dot;', 1),
-    ('prefill_v_from_k', 'V[(size_t)t * head_dim + d] = element(v_pool, first + d, dtype);', 'V[(size_t)t * head_dim + d] = element(k_pool, first + d, dtype);', 1),
+    ('prefill_v_from_k', 'v_scale * element(v_pool, first + d, kv_dtype);', 'v_scale * element(k_pool, first + d, kv_dtype);', 1),
+    ('prefill_k_scale_dropped', 'K[(size_t)t * head_dim + d] = k_scale * element', 'K[(size_t)t * head_dim + d] = element', 1),
+    ('prefill_v_scale_dropped', 'V[(size_t)t * head_dim + d] = v_scale * element', 'V[(size_t)t * head_dim + d] = element', 1),
+    ('prefill_v_with_k_scale', 'V[(size_t)t * head_dim + d] = v_scale * element', 'V[(size_t)t * head_dim + d] = k_scale * element', 1),
+    ('prefill_query_read_as_kv_dtype', 'dot += element(q, qoff + d, q_dtype) * K[(size_t)t * head_dim + d];\n          score[t]', 'dot += element(q, qoff + d, kv_dtype) * K[(size_t)t * head_dim + d];\n          score[t]', 1),
     ('prefill_query_row_of_chunk_start', 'const size_t qoff = ((size_t)(q_starts[s] + i) * num_q_heads + h) * head_dim;', 'const size_t qoff = ((size_t)(q_starts[s]) * num_q_heads + h) * head_dim;', 1),
 ]
 
