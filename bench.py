@@ -336,9 +336,10 @@ def run_ours(args, world, rank, local) -> None:
     ms_per_step = total_ms / args.steps
     eager_ms = statistics.mean(time_steps(step.run, args.steps, flush))
 
-    # ---- the decode call alone (one kernel launch), same stream, L2 flushed
-    dtimes = time_steps(decode_graph.replay, max(args.steps, 10), flush)
-    dec_ms = statistics.mean(dtimes)
+    # ---- the decode call alone (one kernel launch through the C ABI), same stream, L2 flushed;
+    # replayed from a CUDA graph as well (a graph launch of the one kernel measured slower)
+    dec_ms = statistics.mean(time_steps(step.decode, max(args.steps, 10), flush))
+    dec_graph_ms = statistics.mean(time_steps(decode_graph.replay, max(args.steps, 10), flush))
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -376,7 +377,8 @@ def run_ours(args, world, rank, local) -> None:
                      "nominal": {"peak": NOMINAL_HBM_GBS, "unit": "GB/s",
                                  "frac": round(dec_gbs / NOMINAL_HBM_GBS, 4),
                                  "source": "GB300 HBM3e specification (nominal)"},
-                     "algorithmic_bytes": dbytes["total"], "ms_per_launch": round(dec_ms, 4)},
+                     "algorithmic_bytes": dbytes["total"], "ms_per_launch": round(dec_ms, 4),
+                     "ms_per_launch_graph": round(dec_graph_ms, 4)},
         "gpu_launches": step.launches * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(wall, 3),
@@ -492,25 +494,29 @@ def run_prefill_bench(dev, flush, peaks) -> dict:
     """pa_prefill on the GQA geometry (32 q / 8 kv heads x 128, bf16, 16-token blocks):
     16 whole 2,048-token prompts, and 64 chunks of 512 new tokens on 1,536-token histories
     (chunked prefill / recompute); then other head geometries on 8 whole 2,048-token prompts:
-    MHA (32 / 32 x 128, f16), a group of 8 (64 / 8 x 128) and head_dim 64 (32 / 8 x 64).
-    Causal flops per second against the measured bf16 GEMM peak."""
+    MHA (32 / 32 x 128, f16), a group of 8 (64 / 8 x 128) and head_dim 64 (32 / 8 x 64); and the
+    16 prompts over an E4M3 cache with bf16 queries (the FP8 workload's recompute path, f16
+    tensor-core operands). Causal flops per second against the measured bf16 GEMM peak (f16
+    runs at the same dense rate)."""
     import paged_kv_cache_38_gb300 as pa
 
     out = {}
-    for name, lens, chunk, hq, hkv, d, dt in (
-            ("prompts_16x2048", [2048] * 16, 2048, 32, 8, 128, "bf16"),
-            ("chunks_64x512_on_2048", [2048] * 64, 512, 32, 8, 128, "bf16"),
-            ("mha_prompts_8x2048", [2048] * 8, 2048, 32, 32, 128, "f16"),
-            ("g8_prompts_8x2048", [2048] * 8, 2048, 64, 8, 128, "bf16"),
-            ("d64_prompts_8x2048", [2048] * 8, 2048, 32, 8, 64, "bf16")):
-        spec = synth.DecodeSpec(name, len(lens), hq, hkv, d, 16, dt, dt, ctx_lens=tuple(lens))
+    for name, lens, chunk, hq, hkv, d, dt, kvdt in (
+            ("prompts_16x2048", [2048] * 16, 2048, 32, 8, 128, "bf16", "bf16"),
+            ("chunks_64x512_on_2048", [2048] * 64, 512, 32, 8, 128, "bf16", "bf16"),
+            ("mha_prompts_8x2048", [2048] * 8, 2048, 32, 32, 128, "f16", "f16"),
+            ("g8_prompts_8x2048", [2048] * 8, 2048, 64, 8, 128, "bf16", "bf16"),
+            ("d64_prompts_8x2048", [2048] * 8, 2048, 32, 8, 64, "bf16", "bf16"),
+            ("e4m3_prompts_16x2048", [2048] * 16, 2048, 32, 8, 128, "bf16", "e4m3")):
+        spec = synth.DecodeSpec(name, len(lens), hq, hkv, d, 16, kvdt, dt, ctx_lens=tuple(lens))
         case = synth.make_case(spec, seed=SEED, device=dev, logical=False, poison=False)
         n = [chunk] * len(lens)
         qs = torch.tensor(np.concatenate([[0], np.cumsum(n)]), dtype=torch.int32, device=dev)
         q = torch.randn(int(qs[-1]), hq, d, device=dev).to(synth.TORCH_DTYPES[dt])
         o = torch.empty_like(q)
         call = lambda: pa.pa_prefill(q, case.k_pool, case.v_pool, case.block_tables,  # noqa: E731
-                                     case.ctx_lens, qs, case.scale, out=o, max_q_len=chunk)
+                                     case.ctx_lens, qs, case.scale, out=o, max_q_len=chunk,
+                                     k_scale=case.k_scale, v_scale=case.v_scale)
         for _ in range(3):
             call()
         t = statistics.mean(time_steps(call, 10, flush))
@@ -899,18 +905,23 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="time budget of the reference arm's warm-up and timed steps")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill benches and print their result")
     ap.add_argument("--copy-only-layers", type=int, default=0,
                     help="run only the 4,096-pair pa_copy_blocks bench with this many layers "
                          "(a small case for profiling) and print its result")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.copy_only_layers > 0:
+    if args.copy_only_layers > 0 or args.prefill_only:
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
-        print(json.dumps(run_copy_bench(dev, flush, load_peaks(), layers=args.copy_only_layers)))
+        if args.prefill_only:
+            print(json.dumps(run_prefill_bench(dev, flush, load_peaks())))
+        else:
+            print(json.dumps(run_copy_bench(dev, flush, load_peaks(), layers=args.copy_only_layers)))
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -159,8 +159,12 @@ pa_status pa_decode(const pa_decode_args* args, pa_stream stream);
  * A sequence with n > L, L > max_blocks_per_seq * block_size or n above max_q_len rounded up to
  * whole query tiles sets PA_ERR_CTX_LEN and its rows are zero (past that bound they are not
  * written); an out-of-pool block id sets PA_ERR_BLOCK_ID (those rows are then unspecified).
- * Supported: dtype PA_F16 or PA_BF16 (q, K/V and out alike); head_dim 64 or 128; block_size 8,
- * 16, 32 or 64; group size 1, 2, 4, 8 or 16.
+ * Supported: dtype PA_F16 or PA_BF16 (q and out); kv_dtype equal to dtype, or PA_FP8_E4M3
+ * for an FP8 cache ("KV Cache Preemption in vLLM", section "How much KV cache a token costs":
+ * one byte per element), read as K^ = k_scale * value, V^ = v_scale * value (k_scale, v_scale
+ * finite and > 0; head_dim 128), so that a recomputed request of an FP8 cache is prefilled over
+ * the bytes its decode steps read; head_dim 64 or 128; block_size 8, 16, 32 or 64; group size
+ * 1, 2, 4, 8 or 16. A caller that zero-initialises the struct must set kv_dtype.
  * The kernel is persistent (two CTAs per SM). With work_counter set, the call zeroes that int32
  * on the stream and the CTAs take work items from it: the 4 longest query tiles of every
  * (sequence, kv head), then the next 4, and so on; NULL assigns the same items round-robin.
@@ -187,6 +191,9 @@ typedef struct {
   float scale;
   int32_t* err_flag;     /* device int32 or NULL */
   int32_t* work_counter; /* device int32 or NULL, see above */
+  pa_dtype kv_dtype;     /* the pools' element type: dtype, or PA_FP8_E4M3 (see above) */
+  float k_scale;         /* E4M3 cache: K^ = k_scale * stored value (ignored otherwise) */
+  float v_scale;         /* E4M3 cache: V^ = v_scale * stored value (ignored otherwise) */
 } pa_prefill_args;
 
 pa_status pa_prefill(const pa_prefill_args* args, pa_stream stream);

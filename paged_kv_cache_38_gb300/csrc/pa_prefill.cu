@@ -37,6 +37,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 #include <set>
 #include <string>
@@ -59,6 +60,12 @@ constexpr int kSoftmaxWarp0 = 4;  // warps 4..7 form the softmax warpgroup
 constexpr int kItemReaders = 3 + 4;  // K producer, V producer, MMA issuer, 4 softmax warps
 constexpr uint32_t kTmemCols = 256;  // O at columns [0, head_dim), S buffers at [128, 192), [192, 256)
 constexpr uint32_t kCtlBytes = 384;  // barriers, item slots, tensor-memory address, abort flag
+// the E4M3 cache adds the raw-copy barriers, the per-slot query barriers and the per-row query
+// exponents of both item slots
+constexpr uint32_t kCtlBytesFp8 = 640;
+
+// Element type of the K/V pools.
+enum PfKv { kPfF16 = 0, kPfBF16 = 1, kPfE4M3 = 2 };
 
 // Softmax arithmetic on full tiles: 3-input maxima and packed fp32 pairs (fma / add .f32x2)
 // halve the instruction count of the row maximum, the exponent arguments and the row sum; the
@@ -103,7 +110,9 @@ struct PrefillParams {
   int tile_block;    // min(kTileBlock, tiles)
   int pairs;         // num_seqs * num_kv_heads
   int total;         // pairs * tiles rounded up to whole blocks
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // scale * k_scale * log2(e)
+  float v_scale;     // E4M3 cache: stored V value x v_scale (1 otherwise)
+  int out_bf16;      // queries and output are bf16 (else f16)
   unsigned long long wait_ns;  // limit of a wait on another role (1 s unless a test shortened it)
   int stall_cta;     // testing: this CTA's MMA issuer stops after its first S group (-1: none)
 };
@@ -125,11 +134,17 @@ __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   }
 }
 
-template <int D, int G, bool BF16>
+// KV: the pools' element type. An E4M3 cache is widened to f16 in shared memory (every E4M3
+// value is an f16 value) and multiplied on the f16 tensor-core path; bf16 queries are moved to
+// f16 with a power-of-two scale per row (undone in the score scale).
+template <int D, int G, int KV>
 __global__ void __launch_bounds__(kPfThreads, 2)
     pa_prefill_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillParams p) {
+  constexpr bool BF16 = KV == kPfBF16;  // operand type of the MMAs (f16 for F16 and E4M3)
+  constexpr bool kFp8 = KV == kPfE4M3;
+  static_assert(!kFp8 || D == 128, "the E4M3 cache is built for head_dim 128");
   constexpr int kRegions = D / 64;
   constexpr int kTokens = kPfRows / G;
   constexpr uint32_t kQRegion = kPfRows * 128;        // 16 KiB
@@ -175,6 +190,14 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   PfItem* items = reinterpret_cast<PfItem*>(drain + 1);  // [kSlots]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(items + kSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // E4M3 cache only: the raw bytes of tile J land in the upper half of stage J % 2 and
+  // complete on k_raw / v_raw; the producer warp then widens them into the stage and arrives on
+  // k_full / v_full. q_ready[slot] completes when the query tile of the item in that slot is
+  // in f16 and its rows' exponents are in q_exp[slot].
+  uint64_t* k_raw = reinterpret_cast<uint64_t*>(ctl + 256);  // [kPfStages]
+  uint64_t* v_raw = k_raw + kPfStages;                        // [kPfStages]
+  uint64_t* q_ready = v_raw + kPfStages;                      // [kSlots]
+  int8_t* q_exp = reinterpret_cast<int8_t*>(ctl + 384);       // [kSlots][kPfRows]
 
   if (tid == 0) {
     *abort_flag = 0;
@@ -196,6 +219,13 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       mbar_init(smem_addr(item_empty + i), kItemReaders);
     }
     mbar_init(smem_addr(drain), 1);
+    if constexpr (kFp8) {
+      for (int i = 0; i < kPfStages; ++i) {
+        mbar_init(smem_addr(k_raw + i), 1);
+        mbar_init(smem_addr(v_raw + i), 1);
+      }
+      for (int i = 0; i < kSlots; ++i) mbar_init(smem_addr(q_ready + i), 1);
+    }
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -211,95 +241,166 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 
   if (warp == 3) {
     // ------------------------------------------------------------------ items and queries
-    if (lane == 0) {
-      prefetch_tensormap(&qmap);
+    // Lane 0 takes the items and loads their query tiles. With an E4M3 cache the whole warp
+    // then widens each landed tile to f16 (rows lane, lane + 32, ... : one row per lane at a
+    // time) and publishes it on q_ready[slot].
+    if (kFp8 || lane == 0) {
       const uint64_t qpol = policy_evict_first();  // each query tile is read once
+      if (lane == 0) prefetch_tensormap(&qmap);
       int k = 0, fetched = 0;
       for (;;) {
         PfItem it{-1, 0, 0, 0, 0, 0, 0, 0};
-        while (!*abort_flag) {
-          const int v = p.work != nullptr
-                            ? atomicAdd(p.work, 1)
-                            : static_cast<int>(blockIdx.x) + fetched * static_cast<int>(gridDim.x);
-          ++fetched;
-          if (v >= p.total) break;
-          const int per_block = p.pairs * p.tile_block;
-          const int blk = v / per_block, rem = v - blk * per_block;
-          const int sg = rem / p.tile_block;
-          const int tile = p.tiles - 1 - (blk * p.tile_block + (rem - sg * p.tile_block));
-          if (tile < 0) continue;  // past the shortest tile (the last block is partial)
-          const int s = sg / p.num_kv_heads, g = sg - s * p.num_kv_heads;
-          const int q0 = __ldg(p.q_starts + s);
-          const int n = __ldg(p.q_starts + s + 1) - q0;
-          const int t0 = tile * kTokens;
-          if (t0 >= n) continue;  // the chunk is shorter than this tile
-          const int L = __ldg(p.ctx_lens + s);
-          const bool rows_ok = q0 >= 0 && q0 + n <= p.num_tokens;
-          // invalid lengths (or a chunk longer than max_q_len): the tile's rows are zero
-          if (!rows_ok || n > L || L > p.max_blocks * p.block_size || n > p.tiles * kTokens) {
-            flag_error(p.err, kErrCtxLen);
-            if (rows_ok) {
-              const int tend = min(n, t0 + kTokens);
-              for (int t = t0; t < tend; ++t)
-                for (int i = 0; i < G * D / 8; ++i)
-                  reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                           (static_cast<size_t>(q0 + t) * Hq + g * G) * D)[i] =
-                      make_uint4(0, 0, 0, 0);
-            }
-            continue;
-          }
-          // causal extent of the tile: its last query stands at position L - n + t_last
-          const int t_last = min(n, t0 + kTokens) - 1;
-          it = PfItem{s, g, t0, n, L, q0, (L - n + t_last + 1 + kPfKeys - 1) / kPfKeys, 0};
-          break;
-        }
         const int slot = k % kSlots;
-        if (k >= kSlots &&
-            !mbar_wait_bounded(smem_addr(item_empty + slot), ((k / kSlots) - 1) & 1, p.wait_ns)) {
-          fail();
-          it.s = -1;
-        }
-        items[slot] = it;
-        mbar_arrive(smem_addr(item_full + slot));
-        if (it.s < 0) break;
-        // the query buffer is free once the previous item's last S MMA has completed
-        if (k >= 1 && !mbar_wait_bounded(smem_addr(q_empty), (k - 1) & 1, p.wait_ns)) {
-          fail();
-          break;
-        }
-        mbar_arrive_expect_tx(smem_addr(q_full), kRegions * kQRegion);
+        bool loaded = false;
+        if (lane == 0) {
+          while (!*abort_flag) {
+            const int v = p.work != nullptr
+                              ? atomicAdd(p.work, 1)
+                              : static_cast<int>(blockIdx.x) + fetched * static_cast<int>(gridDim.x);
+            ++fetched;
+            if (v >= p.total) break;
+            const int per_block = p.pairs * p.tile_block;
+            const int blk = v / per_block, rem = v - blk * per_block;
+            const int sg = rem / p.tile_block;
+            const int tile = p.tiles - 1 - (blk * p.tile_block + (rem - sg * p.tile_block));
+            if (tile < 0) continue;  // past the shortest tile (the last block is partial)
+            const int s = sg / p.num_kv_heads, g = sg - s * p.num_kv_heads;
+            const int q0 = __ldg(p.q_starts + s);
+            const int n = __ldg(p.q_starts + s + 1) - q0;
+            const int t0 = tile * kTokens;
+            if (t0 >= n) continue;  // the chunk is shorter than this tile
+            const int L = __ldg(p.ctx_lens + s);
+            const bool rows_ok = q0 >= 0 && q0 + n <= p.num_tokens;
+            // invalid lengths (or a chunk longer than max_q_len): the tile's rows are zero
+            if (!rows_ok || n > L || L > p.max_blocks * p.block_size || n > p.tiles * kTokens) {
+              flag_error(p.err, kErrCtxLen);
+              if (rows_ok) {
+                const int tend = min(n, t0 + kTokens);
+                for (int t = t0; t < tend; ++t)
+                  for (int i = 0; i < G * D / 8; ++i)
+                    reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                             (static_cast<size_t>(q0 + t) * Hq + g * G) * D)[i] =
+                        make_uint4(0, 0, 0, 0);
+              }
+              continue;
+            }
+            // causal extent of the tile: its last query stands at position L - n + t_last
+            const int t_last = min(n, t0 + kTokens) - 1;
+            it = PfItem{s, g, t0, n, L, q0, (L - n + t_last + 1 + kPfKeys - 1) / kPfKeys, 0};
+            break;
+          }
+          if (k >= kSlots &&
+              !mbar_wait_bounded(smem_addr(item_empty + slot), ((k / kSlots) - 1) & 1, p.wait_ns)) {
+            fail();
+            it.s = -1;
+          }
+          items[slot] = it;
+          mbar_arrive(smem_addr(item_full + slot));
+          // the query buffer is free once the previous item's last S MMA has completed
+          if (it.s >= 0 &&
+              (k == 0 || mbar_wait_bounded(smem_addr(q_empty), (k - 1) & 1, p.wait_ns))) {
+            mbar_arrive_expect_tx(smem_addr(q_full), kRegions * kQRegion);
 #pragma unroll
-        for (int c = 0; c < kRegions; ++c)
-          tma_load_3d(sQ + c * kQRegion, &qmap, c * 64, it.g * G, it.q0 + it.t0, smem_addr(q_full),
-                      qpol);
-        ++k;
+            for (int c = 0; c < kRegions; ++c)
+              tma_load_3d(sQ + c * kQRegion, &qmap, c * 64, it.g * G, it.q0 + it.t0,
+                          smem_addr(q_full), qpol);
+            loaded = true;
+          } else if (it.s >= 0) {
+            fail();
+          }
+        }
+        if constexpr (kFp8) loaded = __shfl_sync(0xffffffffu, loaded, 0);
+        if (!loaded) break;
+        const int kq = k++;
+        if constexpr (kFp8) {
+          const bool landed =
+              __all_sync(0xffffffffu, mbar_wait_bounded(smem_addr(q_full), kq & 1, p.wait_ns));
+          if (!landed) {
+            if (lane == 0) fail();
+            break;
+          }
+          // bf16 queries: row r times 2^e_r, with e_r putting the row's largest magnitude in
+          // [2^14, 2^15), is exact in f16 for every element above f16's subnormal range
+          for (int r = lane; r < kPfRows; r += 32) {
+            int e = 0;
+            if (p.out_bf16) {
+              float amax = 0.f;
+#pragma unroll
+              for (int c = 0; c < 8 * kRegions; ++c) {
+                const uint4 v = lds128(sQ + (c / 8) * kQRegion + sw128_offset(r, c % 8));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 f = bf16x2_to_float2(w[i]);
+                  amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+              }
+              if (amax > 0.f && amax < INFINITY) e = max(-120, min(120, 14 - ilogbf(amax)));
+              const float up = ldexpf(1.f, e);
+#pragma unroll
+              for (int c = 0; c < 8 * kRegions; ++c) {
+                const uint32_t a = sQ + (c / 8) * kQRegion + sw128_offset(r, c % 8);
+                const uint4 v = lds128(a);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t h[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 f = bf16x2_to_float2(w[i]);
+                  h[i] = pack16<false>(f.x * up, f.y * up);
+                }
+                *reinterpret_cast<uint4*>(bp + (a - base)) = make_uint4(h[0], h[1], h[2], h[3]);
+              }
+            }
+            q_exp[slot * kPfRows + r] = static_cast<int8_t>(e);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(q_ready + slot));
+        }
       }
       // no query copy may still be landing when the CTA exits (matters after an abort)
-      if (k >= 1) mbar_wait_bounded(smem_addr(q_full), (k - 1) & 1, kDrainLimitNs);
+      if (lane == 0 && k >= 1) mbar_wait_bounded(smem_addr(q_full), (k - 1) & 1, kDrainLimitNs);
     }
   } else if (warp == 0 || warp == 2) {
     // ------------------------------------------------------------------ K/V producers
     // warp 0 streams K, warp 2 streams V, each through its own ring (two lanes of one warp
-    // would hold each other up in their barrier waits)
-    if (lane == 0) {
+    // would hold each other up in their barrier waits). Lane 0 issues the copies. With an E4M3
+    // cache the copies bring the raw bytes into the upper half of the stage and the whole warp
+    // then widens them to f16 in place (a raw row sits where its f16 upper half goes, so each
+    // row is read by its lanes before any of them writes).
+    if (kFp8 || lane == 0) {
+      // the warp's decisions must be uniform when all its lanes take part
+      auto all = [](bool v) -> bool {
+        if constexpr (kFp8) return __all_sync(0xffffffffu, v) != 0;
+        return v;
+      };
+      auto any = [](bool v) -> bool {
+        if constexpr (kFp8) return __any_sync(0xffffffffu, v) != 0;
+        return v;
+      };
       const bool is_v = warp == 2;
       const CUtensorMap* map = is_v ? &vmap : &kmap;
       uint64_t* fullb = is_v ? v_full : k_full;
+      uint64_t* rawb = is_v ? v_raw : k_raw;      // E4M3: raw copies landed
+      uint64_t* copyb = kFp8 ? rawb : fullb;      // the barrier the copies complete on
       uint64_t* emptyb = is_v ? o_done : s_full;  // stage st of tile J - 2 consumed
       const uint64_t pol = policy_evict_normal();  // the sequence's other query tiles reread them
       const int urows = 1 << p.log2_urows, B = p.block_size;
       const int units = kPfKeys >> p.log2_urows;
-      prefetch_tensormap(map);
+      // bytes of one copy unit, and where a tile's copies land within the stage
+      constexpr uint32_t kUnitRowBytes = kFp8 ? 128u : static_cast<uint32_t>(kRegions) * 128u;
+      constexpr uint32_t kLandOffset = kFp8 ? kKVRegion : 0u;
+      if (lane == 0) prefetch_tensormap(map);
       int J = 0;  // tiles issued, over all items
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int slot = k % kSlots;
-        if (!mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1, p.wait_ns)) {
-          fail();
+        if (!all(mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1, p.wait_ns))) {
+          if (lane == 0) fail();
           break;
         }
         const PfItem it = items[slot];
-        if (it.s < 0 || *abort_flag) break;
+        if (any(it.s < 0 || *abort_flag)) break;
         const int32_t* trow = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks;
         // The block-table entries of tile j + 1 are read while the producer waits for a free
         // stage for tile j + 1, so their latency is off the copy path.
@@ -315,47 +416,92 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         for (int j = 0; j < it.ntiles; ++j, ++J) {
           const int st = J % kPfStages;
           if (J >= kPfStages &&
-              !mbar_wait_bounded(smem_addr(emptyb + st), ((J / kPfStages) - 1) & 1, p.wait_ns)) {
-            fail();
+              !all(mbar_wait_bounded(smem_addr(emptyb + st), ((J / kPfStages) - 1) & 1,
+                                     p.wait_ns))) {
+            if (lane == 0) fail();
             ok = false;
             break;
           }
-          if (*abort_flag) {
+          if (any(*abort_flag)) {
             ok = false;
             break;
           }
-          int rowc[8];
-          uint32_t bytes = 0;
+          const uint32_t dst = sKV + 2 * st * kKVBytes + (is_v ? kKVBytes : 0u);
+          if (lane == 0) {
+            int rowc[8];
+            uint32_t bytes = 0;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int key = j * kPfKeys + u * urows;
-            rowc[u] = -1;
-            if (ph[u] == -2) continue;  // past the unit count or the cache
-            if (ph[u] < 0 || ph[u] >= p.num_blocks) {
-              if (!is_v) flag_error(p.err, kErrBlockId);
-            } else {
-              rowc[u] = (ph[u] * p.num_kv_heads + it.g) * B + (key & (B - 1));
-              bytes += static_cast<uint32_t>(kRegions * urows * 128);
+            for (int u = 0; u < 8; ++u) {
+              const int key = j * kPfKeys + u * urows;
+              rowc[u] = -1;
+              if (ph[u] == -2) continue;  // past the unit count or the cache
+              if (ph[u] < 0 || ph[u] >= p.num_blocks) {
+                if (!is_v) flag_error(p.err, kErrBlockId);
+              } else {
+                rowc[u] = (ph[u] * p.num_kv_heads + it.g) * B + (key & (B - 1));
+                bytes += kUnitRowBytes * static_cast<uint32_t>(urows);
+              }
+            }
+            const uint32_t bar = smem_addr(copyb + st);
+            mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (rowc[u] < 0) continue;
+              if constexpr (kFp8) {
+                tma_load_2d(dst + kLandOffset + static_cast<uint32_t>(u * urows * 128), map, 0,
+                            rowc[u], bar, pol);
+              } else {
+#pragma unroll
+                for (int c = 0; c < kRegions; ++c)
+                  tma_load_2d(dst + c * kKVRegion + static_cast<uint32_t>(u * urows * 128), map,
+                              c * 64, rowc[u], bar, pol);
+              }
             }
           }
-          const uint32_t full = smem_addr(fullb + st);
-          mbar_arrive_expect_tx(full, bytes);
-          const uint32_t dst = sKV + 2 * st * kKVBytes + (is_v ? kKVBytes : 0u);
+          if constexpr (kFp8) {
+            // widen the tile: lane (row r % 4 of a group of 4 rows, 16-byte chunk c) turns 16
+            // E4M3 values into two 16-byte f16 chunks of the row's region c / 4
+            if (!all(mbar_wait_bounded(smem_addr(rawb + st), (J / kPfStages) & 1, p.wait_ns))) {
+              if (lane == 0) fail();
+              ok = false;
+              ++J;  // its copies were issued: the drain below waits for them
+              break;
+            }
+            const int rr = lane >> 3, c = lane & 7;
+            uint8_t* stage = bp + (dst - base);
+#pragma unroll 4
+            for (int r0 = 0; r0 < kPfKeys; r0 += 4) {
+              const int r = r0 + rr;
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(stage + kLandOffset + sw128_offset(r, c));
+              __syncwarp();
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+              uint32_t h[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (rowc[u] < 0) continue;
-#pragma unroll
-            for (int c = 0; c < kRegions; ++c)
-              tma_load_2d(dst + c * kKVRegion + static_cast<uint32_t>(u * urows * 128), map,
-                          c * 64, rowc[u], full, pol);
+              for (int i = 0; i < 4; ++i) {
+                h[2 * i] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] & 0xffffu));
+                h[2 * i + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i] >> 16));
+              }
+              uint8_t* region = stage + (c >> 2) * kKVRegion;
+              const int c0 = 2 * (c & 3);
+              *reinterpret_cast<uint4*>(region + sw128_offset(r, c0)) =
+                  make_uint4(h[0], h[1], h[2], h[3]);
+              *reinterpret_cast<uint4*>(region + sw128_offset(r, c0 + 1)) =
+                  make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(fullb + st));
           }
           if (j + 1 < it.ntiles) load_phys(j + 1);
         }
-        if (ok) mbar_arrive(smem_addr(item_empty + slot));
+        if (ok && lane == 0) mbar_arrive(smem_addr(item_empty + slot));
       }
       // no copy of this CTA may still be landing when it exits (matters after an abort)
-      for (int jj = max(0, J - kPfStages); jj < J; ++jj)
-        mbar_wait_bounded(smem_addr(fullb + jj % kPfStages), (jj / kPfStages) & 1, kDrainLimitNs);
+      if (lane == 0)
+        for (int jj = max(0, J - kPfStages); jj < J; ++jj)
+          mbar_wait_bounded(smem_addr(copyb + jj % kPfStages), (jj / kPfStages) & 1,
+                            kDrainLimitNs);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -440,7 +586,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           const int st = ns % kPfStages, b = ns & 1;
           if (mbar_test(smem_addr(k_full + st), (ns / kPfStages) & 1) &&
               (ns < 2 || mbar_test(smem_addr(s_free + b), ((ns >> 1) - 1) & 1)) &&
-              (jS > 0 || mbar_test(smem_addr(q_full), kS & 1))) {
+              (jS > 0 || (kFp8 ? mbar_test(smem_addr(q_ready + kS % kSlots), (kS / kSlots) & 1)
+                                : mbar_test(smem_addr(q_full), kS & 1)))) {
             tc_fence_after();
             const uint64_t dKs = dK + ((2u * st * kKVBytes) >> 4);
             const uint32_t dS = tS + 64 * b;
@@ -488,6 +635,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     float pend_inv = 0.f;
     uint4* pend_dst = nullptr;
     int pend_slot = 0;
+    // output rows in the query dtype: the MMA operand type, except for an E4M3 cache (f16
+    // operands, bf16 or f16 output)
+    auto pack_out = [&](float lo, float hi) -> uint32_t {
+      if constexpr (kFp8) return p.out_bf16 ? pack16<true>(lo, hi) : pack16<false>(lo, hi);
+      return pack16<BF16>(lo, hi);
+    };
     auto epilogue = [&]() {
       // two 32-column loads per wait: each tensor-memory round trip is on the item's path
 #pragma unroll 1
@@ -502,8 +655,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              w[i] = pack16<BF16>(__uint_as_float(v[h][2 * i]) * pend_inv,
-                                  __uint_as_float(v[h][2 * i + 1]) * pend_inv);
+              w[i] = pack_out(__uint_as_float(v[h][2 * i]) * pend_inv,
+                              __uint_as_float(v[h][2 * i + 1]) * pend_inv);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               pend_dst[(c + 32 * h) / 8 + i] =
@@ -522,12 +675,23 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     for (int k = 0;; ++k) {
       const int slot = k % kSlots;
       ok = mbar_wait_bounded(smem_addr(item_full + slot), (k / kSlots) & 1, p.wait_ns);
-      if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
+      if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
         ok = false;
         break;
       }
       const PfItem it = items[slot];
       if (it.s < 0) break;
+      // scores are scaled into the log2 domain by scale * k_scale * log2(e), and, for queries
+      // widened from bf16, by the row's 2^-e as well
+      float row_scale = p.scale_log2;
+      if constexpr (kFp8) {
+        ok = mbar_wait_bounded(smem_addr(q_ready + slot), (k / kSlots) & 1, p.wait_ns);
+        if (__any_sync(0xffffffffu, !ok)) {
+          ok = false;
+          break;
+        }
+        row_scale = ldexpf(p.scale_log2, -static_cast<int>(q_exp[slot * kPfRows + r]));
+      }
       const int tr = it.t0 + r / G;
       const bool row_valid = tr < it.n;
       const int pos = it.L - it.n + tr;  // last position this row may see
@@ -535,7 +699,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       for (int j = 0; j < it.ntiles; ++j, ++jx) {
         const int b = jx & 1;
         ok = mbar_wait_bounded(smem_addr(s_full + b), (jx >> 1) & 1, p.wait_ns);
-        if (__any_sync(0xffffffffu, !ok) || *abort_flag) {
+        if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
           ok = false;
           break;
         }
@@ -580,7 +744,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           for (int c = 0; c < kPfKeys; ++c)
             if (c <= lim) mt = fmaxf(mt, x[c]);
         }
-        mt = mt == -INFINITY ? -INFINITY : mt * p.scale_log2;
+        mt = mt == -INFINITY ? -INFINITY : mt * row_scale;
         // Lazy rescaling: the row keeps its reference maximum m unless the tile's maximum
         // exceeds it by more than 8 (log2 units); weights then stay below 2^8 and O is rescaled
         // rarely. Numerator and denominator share the same reference, so the result is
@@ -591,7 +755,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         float psum = 0.f;
         if (full) {
           // pairs of scores through one packed FMA; the row sum in two packed partial sums
-          const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2), nm2 = f2pack(-m_new, -m_new);
+          const uint64_t sc2 = f2pack(row_scale, row_scale), nm2 = f2pack(-m_new, -m_new);
           uint64_t s2 = f2pack(0.f, 0.f);
 #pragma unroll
           for (int c = 0; c < kPfKeys; c += 2) {
@@ -608,9 +772,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
 #pragma unroll
           for (int c = 0; c < kPfKeys; c += 2) {
             const float p0 =
-                c <= lim && m_new != -INFINITY ? ex2(fmaf(x[c], p.scale_log2, -m_new)) : 0.f;
+                c <= lim && m_new != -INFINITY ? ex2(fmaf(x[c], row_scale, -m_new)) : 0.f;
             const float p1 = c + 1 <= lim && m_new != -INFINITY
-                                 ? ex2(fmaf(x[c + 1], p.scale_log2, -m_new))
+                                 ? ex2(fmaf(x[c + 1], row_scale, -m_new))
                                  : 0.f;
             pk[c / 2] = pack16<BF16>(p0, p1);
             psum += p0 + p1;
@@ -671,7 +835,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       // ---- the item's epilogue is deferred (see above)
       pend = true;
       pend_valid = row_valid;
-      pend_inv = l > 0.f ? 1.f / l : 0.f;
+      if constexpr (kFp8)
+        pend_inv = l > 0.f ? p.v_scale / l : 0.f;
+      else
+        pend_inv = l > 0.f ? 1.f / l : 0.f;
       pend_dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
                                           (static_cast<size_t>(it.q0 + tr) * Hq + it.g * G + r % G) * D);
       pend_slot = slot;
@@ -705,10 +872,10 @@ std::set<std::pair<const void*, int>>& pf_opted() {
   return s;
 }
 
-template <int D, int G, bool BF16>
+template <int D, int G, int KV>
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                            const PrefillParams& p, unsigned grid, size_t smem, cudaStream_t stream) {
-  auto fn = pa_prefill_kernel<D, G, BF16>;
+  auto fn = pa_prefill_kernel<D, G, KV>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -726,16 +893,16 @@ cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const C
   return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, int KV>
 cudaError_t launch_prefill_g(int group, const CUtensorMap& qm, const CUtensorMap& km,
                              const CUtensorMap& vm, const PrefillParams& p, unsigned grid,
                              size_t smem, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_prefill<D, 1, BF16>(qm, km, vm, p, grid, smem, stream);
-    case 2: return launch_prefill<D, 2, BF16>(qm, km, vm, p, grid, smem, stream);
-    case 4: return launch_prefill<D, 4, BF16>(qm, km, vm, p, grid, smem, stream);
-    case 8: return launch_prefill<D, 8, BF16>(qm, km, vm, p, grid, smem, stream);
-    default: return launch_prefill<D, 16, BF16>(qm, km, vm, p, grid, smem, stream);
+    case 1: return launch_prefill<D, 1, KV>(qm, km, vm, p, grid, smem, stream);
+    case 2: return launch_prefill<D, 2, KV>(qm, km, vm, p, grid, smem, stream);
+    case 4: return launch_prefill<D, 4, KV>(qm, km, vm, p, grid, smem, stream);
+    case 8: return launch_prefill<D, 8, KV>(qm, km, vm, p, grid, smem, stream);
+    default: return launch_prefill<D, 16, KV>(qm, km, vm, p, grid, smem, stream);
   }
 }
 
@@ -754,12 +921,26 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   }
   const int group = a.num_q_heads / a.num_kv_heads;
   if (a.dtype != PA_F16 && a.dtype != PA_BF16) {
-    msg = "pa_prefill supports PA_F16 and PA_BF16";
+    msg = "pa_prefill supports PA_F16 and PA_BF16 queries";
     return PA_EUNSUPPORTED;
+  }
+  const bool fp8 = a.kv_dtype == PA_FP8_E4M3;
+  if (!fp8 && a.kv_dtype != a.dtype) {
+    msg = "kv_dtype must equal dtype, or be PA_FP8_E4M3";
+    return PA_EINVAL;
   }
   if (a.head_dim != 64 && a.head_dim != 128) {
     msg = "head_dim must be 64 or 128";
     return PA_EUNSUPPORTED;
+  }
+  if (fp8 && a.head_dim != 128) {
+    msg = "an E4M3 cache is built for head_dim 128";
+    return PA_EUNSUPPORTED;
+  }
+  if (fp8 && (!(a.k_scale > 0.f) || !(a.v_scale > 0.f) || !std::isfinite(a.k_scale) ||
+              !std::isfinite(a.v_scale))) {
+    msg = "k_scale and v_scale must be finite and > 0 for an E4M3 cache";
+    return PA_EINVAL;
   }
   if (a.block_size != 8 && a.block_size != 16 && a.block_size != 32 && a.block_size != 64) {
     msg = "pa_prefill supports block_size 8, 16, 32 or 64";
@@ -801,9 +982,10 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   pa_status st = encode_query_tile_map(&qmap, a.q, a.num_tokens, a.num_q_heads, a.head_dim, group,
                                        tokens_per_tile, msg);
   if (st != PA_OK) return st;
-  st = encode_pool_rows_map(&kmap, a.k_pool, rows, a.head_dim, 2, urows, msg);
+  const int elt = fp8 ? 1 : 2;
+  st = encode_pool_rows_map(&kmap, a.k_pool, rows, a.head_dim, elt, urows, msg);
   if (st != PA_OK) return st;
-  st = encode_pool_rows_map(&vmap, a.v_pool, rows, a.head_dim, 2, urows, msg);
+  st = encode_pool_rows_map(&vmap, a.v_pool, rows, a.head_dim, elt, urows, msg);
   if (st != PA_OK) return st;
 
   PrefillParams p{};
@@ -827,7 +1009,9 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   p.tile_block = static_cast<int>(tile_block);
   p.pairs = a.num_seqs * a.num_kv_heads;
   p.total = static_cast<int>(total);
-  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.scale_log2 = a.scale * (fp8 ? a.k_scale : 1.f) * 1.4426950408889634f;
+  p.v_scale = fp8 ? a.v_scale : 1.f;
+  p.out_bf16 = a.dtype == PA_BF16 ? 1 : 0;
   p.wait_ns = launch_wait_ns();
   p.stall_cta = launch_stall_cta();
 
@@ -836,7 +1020,7 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   // no alignment slack: the kernel needs (and checks) a 1024-byte aligned dynamic region, and
   // two CTAs then fit on an SM
   const size_t smem = regions * kPfRows * 128 + kPfStages * 2 * regions * kPfKeys * 128 +
-                      kPfRows * 128 + kCtlBytes;
+                      kPfRows * 128 + (fp8 ? kCtlBytesFp8 : kCtlBytes);
   const int sms = device_sm_count();
   if (sms <= 0) {
     msg = "cannot read the SM count of the current device";
@@ -850,12 +1034,14 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   }
   const bool bf16 = a.dtype == PA_BF16;
   cudaError_t e;
-  if (D == 128)
-    e = bf16 ? launch_prefill_g<128, true>(group, qmap, kmap, vmap, p, grid, smem, stream)
-             : launch_prefill_g<128, false>(group, qmap, kmap, vmap, p, grid, smem, stream);
+  if (fp8)
+    e = launch_prefill_g<128, kPfE4M3>(group, qmap, kmap, vmap, p, grid, smem, stream);
+  else if (D == 128)
+    e = bf16 ? launch_prefill_g<128, kPfBF16>(group, qmap, kmap, vmap, p, grid, smem, stream)
+             : launch_prefill_g<128, kPfF16>(group, qmap, kmap, vmap, p, grid, smem, stream);
   else
-    e = bf16 ? launch_prefill_g<64, true>(group, qmap, kmap, vmap, p, grid, smem, stream)
-             : launch_prefill_g<64, false>(group, qmap, kmap, vmap, p, grid, smem, stream);
+    e = bf16 ? launch_prefill_g<64, kPfBF16>(group, qmap, kmap, vmap, p, grid, smem, stream)
+             : launch_prefill_g<64, kPfF16>(group, qmap, kmap, vmap, p, grid, smem, stream);
   return cuda_status(e, "pa_prefill kernel launch", msg);
 }
 

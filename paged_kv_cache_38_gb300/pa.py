@@ -201,7 +201,8 @@ class pa_prefill_args(ctypes.Structure):
         ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
         ("max_blocks_per_seq", ctypes.c_int32), ("max_q_len", ctypes.c_int32),
         ("dtype", ctypes.c_int), ("scale", ctypes.c_float), ("err_flag", ctypes.c_void_p),
-        ("work_counter", ctypes.c_void_p),
+        ("work_counter", ctypes.c_void_p), ("kv_dtype", ctypes.c_int),
+        ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
     ]
 
 
@@ -210,12 +211,14 @@ def pa_prefill(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                scale: float, *, out: Optional[torch.Tensor] = None,
                max_q_len: Optional[int] = None, err_flag: Optional[torch.Tensor] = None,
                work_counter: Optional[torch.Tensor] = None, dynamic: bool = True,
-               stream=None) -> torch.Tensor:
+               k_scale: float = 1.0, v_scale: float = 1.0, stream=None) -> torch.Tensor:
     """Causal attention of each sequence's chunk of query tokens (rows q_starts[s] ..
     q_starts[s + 1] - 1 of q [num_tokens][num_q_heads][head_dim]) over its paged cache.
 
-    dynamic: the persistent CTAs take work items from an int32 counter (work_counter, or one
-    allocated for the call); False assigns them round-robin."""
+    Pools of uint8 (or float8_e4m3fn) are an E4M3 cache read as value x k_scale / v_scale;
+    otherwise they have the query dtype. dynamic: the persistent CTAs take work items from an
+    int32 counter (work_counter, or one allocated for the call); False assigns them
+    round-robin."""
     if out is None:
         out = torch.empty_like(q)
     dt = {torch.float16: PA_F16, torch.bfloat16: PA_BF16}.get(q.dtype)
@@ -232,6 +235,8 @@ def pa_prefill(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
     a.num_kv_heads, a.block_size, a.num_blocks = k_pool.shape[1], k_pool.shape[2], k_pool.shape[0]
     a.max_blocks_per_seq = block_tables.shape[1] if block_tables.dim() == 2 else 0
     a.max_q_len, a.dtype, a.scale = int(max_q_len), dt, float(scale)
+    a.kv_dtype = kv_dtype_code(k_pool)
+    a.k_scale, a.v_scale = float(k_scale), float(v_scale)
     a.err_flag = _ptr(err_flag)
     if dynamic and work_counter is None:
         work_counter = torch.empty(1, dtype=torch.int32, device=q.device)

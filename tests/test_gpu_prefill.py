@@ -3,6 +3,8 @@
 Each sequence's chunk of n new tokens stands at its last n cache positions and attends
 causally; whole prompts (n = L), partial chunks and one-token chunks; stale slots and free
 blocks hold NaN, so any read past a sequence's context shows."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -21,6 +23,10 @@ SPECS = [
     synth.DecodeSpec("pf_bf16_g8_d64_b32", 5, 16, 2, 64, 32, "bf16", "bf16", ctx_range=(1, 200)),
     synth.DecodeSpec("pf_f16_g16_b64", 3, 32, 2, 128, 64, "f16", "f16", ctx_range=(1, 330)),
     synth.DecodeSpec("pf_bf16_g2_d64_b8", 5, 8, 4, 64, 8, "bf16", "bf16", ctx_range=(1, 150)),
+    # an E4M3 cache (per-tensor k_scale / v_scale) with bf16 and with f16 queries
+    synth.DecodeSpec("pf_e4m3_g4_b16", 6, 32, 8, 128, 16, "e4m3", "bf16", ctx_range=(1, 300)),
+    synth.DecodeSpec("pf_e4m3_g1_b32_f16q", 4, 4, 4, 128, 32, "e4m3", "f16", ctx_range=(1, 260)),
+    synth.DecodeSpec("pf_e4m3_g16_b8", 3, 32, 2, 128, 8, "e4m3", "bf16", ctx_range=(1, 200)),
 ]
 CHUNKS = ["whole", "partial", "one"]
 
@@ -29,9 +35,10 @@ def _oracle(case, qs, q):
     spec = case.spec
     return oracle.load().prefill(q.cpu(), case.k_pool.cpu(), case.v_pool.cpu(),
                                  case.block_tables.cpu(), case.ctx_lens.cpu(), qs.cpu(),
-                                 dtype=spec.kv_dtype, num_q_heads=spec.num_q_heads,
-                                 num_kv_heads=spec.num_kv_heads, head_dim=spec.head_dim,
-                                 block_size=spec.block_size, scale=case.scale)
+                                 dtype=spec.kv_dtype, q_dtype=spec.q_dtype,
+                                 num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                                 head_dim=spec.head_dim, block_size=spec.block_size,
+                                 scale=case.scale, k_scale=case.k_scale, v_scale=case.v_scale)
 
 
 def _err(out, ref):
@@ -49,7 +56,7 @@ def test_prefill_matches_oracle(spec, chunk):
     g = case.to("cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qs.cuda(),
-                        case.scale, err_flag=err)
+                        case.scale, err_flag=err, k_scale=case.k_scale, v_scale=case.v_scale)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     e = _err(out, ref)
@@ -252,3 +259,44 @@ def test_prefill_out_of_pool_block_flagged():
     keep = torch.cat([out[:lo], out[hi:]])
     want = np.concatenate([ref[:lo], ref[hi:]])
     assert _err(keep, want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("log2_mag", [16, -20])
+def test_prefill_e4m3_queries_beyond_f16_range(log2_mag):
+    """bf16 queries scaled by 2^16 (above f16's largest value) or 2^-20 (below its normal range),
+    with the softmax scale divided by the same power of two: the scores are those of the
+    unscaled queries, exactly. The kernel moves each query row to f16 with its own power-of-two
+    scale, so both match the oracle (which reads the bf16 values exactly); a plain conversion
+    would overflow or lose the small values."""
+    spec = synth.DecodeSpec("pf_e4m3_mag", 4, 32, 8, 128, 16, "e4m3", "bf16", ctx_range=(40, 400))
+    case = synth.make_case(spec, seed=77)
+    qs, q = synth.prefill_queries(case, seed=5, whole=True)
+    q = (q.float() * 2.0 ** log2_mag).to(torch.bfloat16)  # exact: a power of two
+    case = dataclasses.replace(case, scale=case.scale * 2.0 ** -log2_mag)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qs.cuda(),
+                        case.scale, err_flag=err, k_scale=case.k_scale, v_scale=case.v_scale)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert _err(out, ref) <= TOL["e4m3"]
+
+
+def test_prefill_e4m3_recompute_matches_decode():
+    """A recomputed request of the FP8 workload: its whole history is prefilled over the E4M3
+    cache, and the last row of the chunk equals what pa_decode computes for that position."""
+    spec = synth.SPECS["fp8_long"].scaled(num_seqs=6, ctx_range=(300, 1500))
+    case = synth.make_case(spec, seed=78)
+    qs, q = synth.prefill_queries(case, seed=6, whole=True)
+    ref = _oracle(case, qs, q)
+    g = case.to("cuda")
+    out = pa.pa_prefill(q.cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, qs.cuda(),
+                        case.scale, k_scale=case.k_scale, v_scale=case.v_scale)
+    last = (qs[1:] - 1).long()
+    dec = pa.pa_decode(q[last].cuda(), g.k_pool, g.v_pool, g.block_tables, g.ctx_lens, case.scale,
+                       k_scale=case.k_scale, v_scale=case.v_scale)
+    torch.cuda.synchronize()
+    assert _err(out, ref) <= TOL["e4m3"]
+    assert _err(dec, ref[last.numpy()]) <= TOL["e4m3"]
+    assert float((out[last.cuda()].float() - dec.float()).abs().max()) <= 2 * TOL["e4m3"]
