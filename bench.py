@@ -336,10 +336,25 @@ def run_ours(args, world, rank, local) -> None:
     ms_per_step = total_ms / args.steps
     eager_ms = statistics.mean(time_steps(step.run, args.steps, flush))
 
-    # ---- the decode call alone (one kernel launch through the C ABI), same stream, L2 flushed;
-    # replayed from a CUDA graph as well (a graph launch of the one kernel measured slower)
-    dec_ms = statistics.mean(time_steps(step.decode, max(args.steps, 10), flush))
-    dec_graph_ms = statistics.mean(time_steps(decode_graph.replay, max(args.steps, 10), flush))
+    # ---- the decode call alone (one kernel launch through the C ABI), same stream.
+    # (a) Back to back, no flush in between: the inputs (the pool) are 5x the L2, so each
+    # launch streams its bytes from DRAM; a launch's setup overlaps the previous launch, as in a
+    # serving loop. This is the kernel's per-launch time (it matches the kernel duration ncu
+    # reports) and the roofline's denominator.
+    reps = max(args.steps, 10)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step.decode()
+    a.record()
+    for _ in range(reps):
+        step.decode()
+    b.record()
+    b.synchronize()
+    dec_b2b_ms = a.elapsed_time(b) / reps
+    # (b) Each launch alone after an L2 flush (eager, and replayed from a CUDA graph): adds the
+    # ~5 us an isolated launch takes to start after the flush kernel (an empty kernel of the
+    # same grid measures 4.8 us between events there); reported beside.
+    dec_ms = statistics.mean(time_steps(step.decode, reps, flush))
+    dec_graph_ms = statistics.mean(time_steps(decode_graph.replay, reps, flush))
 
     # ---- end to end through the public API from pinned host buffers
     e2e = None
@@ -348,7 +363,8 @@ def run_ours(args, world, rank, local) -> None:
 
     peaks = load_peaks()
     value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
-    dec_gbs = dbytes["total"] / (dec_ms * 1e-3) / 1e9
+    dec_gbs = dbytes["total"] / (dec_b2b_ms * 1e-3) / 1e9
+    dec_flush_gbs = dbytes["total"] / (dec_ms * 1e-3) / 1e9
     extra = {}
     if rank == 0 and not args.quick:
         extra = run_extras(args, dev, flush, peaks)
@@ -377,8 +393,16 @@ def run_ours(args, world, rank, local) -> None:
                      "nominal": {"peak": NOMINAL_HBM_GBS, "unit": "GB/s",
                                  "frac": round(dec_gbs / NOMINAL_HBM_GBS, 4),
                                  "source": "GB300 HBM3e specification (nominal)"},
-                     "algorithmic_bytes": dbytes["total"], "ms_per_launch": round(dec_ms, 4),
-                     "ms_per_launch_graph": round(dec_graph_ms, 4)},
+                     "algorithmic_bytes": dbytes["total"],
+                     "ms_per_launch": round(dec_b2b_ms, 4),
+                     "timing": f"{reps} launches back to back, CUDA events on the launch stream; "
+                               "pool 5x L2, not flushed between launches",
+                     "after_l2_flush": {
+                         "ms_per_launch": round(dec_ms, 4),
+                         "ms_per_launch_graph": round(dec_graph_ms, 4),
+                         "achieved": round(dec_flush_gbs, 1),
+                         "frac": round(dec_flush_gbs / peaks["hbm_gbs"], 4),
+                         "timing": "each launch alone, L2 flushed before it (outside the events)"}},
         "gpu_launches": step.launches * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": round(wall, 3),
@@ -461,12 +485,23 @@ def run_extras(args, dev, flush, peaks) -> dict:
         st = Step(case, split)
         for _ in range(3):
             st.decode()
-        t = statistics.mean(time_steps(st.decode, 10, flush))
+        # back to back (pools larger than L2), as the main roofline; after an L2 flush beside
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(20):
+            st.decode()
+        e.record()
+        e.synchronize()
+        t = a.elapsed_time(e) / 20
+        tf = statistics.mean(time_steps(st.decode, 10, flush))
         b = decode_bytes(case, split)
         res[name] = {"decode_ms": round(t, 4), "gbs": round(b["total"] / (t * 1e-3) / 1e9, 1),
                      "pct_of_peak": round(100 * b["total"] / (t * 1e-3) / 1e9 / peaks["hbm_gbs"], 1),
                      "pct_of_nominal": round(100 * b["total"] / (t * 1e-3) / 1e9 / NOMINAL_HBM_GBS, 1),
                      "tokens_per_s": round(spec.num_seqs / (t * 1e-3), 1),
+                     "decode_ms_after_l2_flush": round(tf, 4),
+                     "pct_of_peak_after_l2_flush":
+                         round(100 * b["total"] / (tf * 1e-3) / 1e9 / peaks["hbm_gbs"], 1),
                      "split_tokens": split, "bytes": b["total"]}
         del case, st
         torch.cuda.empty_cache()

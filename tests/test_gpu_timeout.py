@@ -23,6 +23,9 @@ import paged_kv_cache_38_gb300 as pa  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 SHORT_NS = 200_000  # 200 us: far longer than any wait of these small cases, far below 1 s
+# A launch that gave up under the shortened limit returns well before the one-second default
+# could have expired once (the kernel is loaded and warm before any timed call).
+FAST_S = 0.9
 
 
 @pytest.fixture(autouse=True)
@@ -71,7 +74,7 @@ def test_decode_grid_barrier_wait_expires(name):
         torch.cuda.synchronize()
         elapsed = time.perf_counter() - t0
         assert int(err.item()) & pa.PA_ERR_TIMEOUT
-        assert elapsed < 0.5, f"the shortened limit was not applied ({elapsed:.3f} s)"
+        assert elapsed < FAST_S, f"the shortened limit was not applied ({elapsed:.3f} s)"
         # the last CTA to finish cleared the three work counters even though the launch gave up
         assert int(ws[:24].count_nonzero().item()) == 0
 
@@ -139,13 +142,15 @@ def test_prefill_waits_expire_when_mma_issuer_stalls():
     CTA frees its tensor memory before returning."""
     g, qs, q, ref = _prefill_case()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _prefill(g, qs, q, err)  # load and warm the kernel before anything is timed
+    torch.cuda.synchronize()
     pa.pa_testing_set_wait_limit(SHORT_NS, 0)
     for _ in range(2):
         err.zero_()
         t0 = time.perf_counter()
         _prefill(g, qs, q, err)
         torch.cuda.synchronize()
-        assert time.perf_counter() - t0 < 0.5
+        assert time.perf_counter() - t0 < FAST_S
         assert int(err.item()) & pa.PA_ERR_TIMEOUT
     pa.pa_testing_set_wait_limit(0, -1)
     err.zero_()
