@@ -338,3 +338,42 @@ def test_execute_moves_matches_oracle_on_whole_pools():
         assert np.array_equal(gk[l].cpu().numpy().reshape(-1), kps[l])
         assert np.array_equal(gv[l].cpu().numpy().reshape(-1), vps[l])
     assert np.array_equal(gcpu.numpy().reshape(-1), cpu)
+
+
+def test_execute_moves_many_pairs_across_launches():
+    """More swap and copy pairs than one launch carries (1,024 per launch): 1,500 copies and
+    1,100 swap-outs then 1,100 swap-ins over 2 layers equal the oracle's pools byte for byte."""
+    from paged_kv_cache_38_gb300 import scheduler as sch
+
+    orc = oracle.load()
+    rng = np.random.default_rng(91)
+    L, nblk, ncpu, bb = 2, 6000, 1200, 1024
+    kps = [rng.integers(0, 256, nblk * bb, dtype=np.uint8) for _ in range(L)]
+    vps = [rng.integers(0, 256, nblk * bb, dtype=np.uint8) for _ in range(L)]
+    cpu = rng.integers(0, 256, ncpu * L * 2 * bb, dtype=np.uint8)
+    perm = rng.permutation(nblk)
+    slots = rng.permutation(ncpu)
+    swap_out = np.stack([perm[:1100], slots[:1100]], 1).astype(np.int32)
+    back = rng.permutation(1100)
+    swap_in = np.stack([slots[:1100][back], perm[1100:2200]], 1).astype(np.int32)
+    copies = np.stack([perm[2200:3700], perm[3700:5200]], 1).astype(np.int32)
+    gk = [torch.from_numpy(p.copy()).cuda().view(nblk, -1) for p in kps]
+    gv = [torch.from_numpy(p.copy()).cuda().view(nblk, -1) for p in vps]
+    gcpu = torch.from_numpy(cpu.copy()).view(ncpu, L, 2, bb).pin_memory()
+    plan = sch.Plan(*([np.zeros(0, np.int64)] + [np.zeros((0, 1), np.int32)]
+                      + [np.zeros(0, np.int32)] * 3 + [np.zeros(0, np.int64)]
+                      + [copies, swap_out, swap_in, [], [], 0]))
+    sch.execute_moves(plan, gk, gv, gcpu)
+    torch.cuda.synchronize()
+    per_slot = L * 2 * bb
+    for b, c in swap_out:
+        assert orc.swap_blocks(kps, vps, cpu[c * per_slot:(c + 1) * per_slot], [b], block_bytes=bb,
+                               direction="out") == 0
+    for c, b in swap_in:
+        assert orc.swap_blocks(kps, vps, cpu[c * per_slot:(c + 1) * per_slot], [b], block_bytes=bb,
+                               direction="in") == 0
+    assert orc.copy_blocks(kps, vps, copies, block_bytes=bb) == 0
+    for l in range(L):
+        assert np.array_equal(gk[l].cpu().numpy().reshape(-1), kps[l])
+        assert np.array_equal(gv[l].cpu().numpy().reshape(-1), vps[l])
+    assert np.array_equal(gcpu.numpy().reshape(-1), cpu)

@@ -4,6 +4,7 @@ Each sequence's chunk of n new tokens stands at its last n cache positions and a
 causally; whole prompts (n = L), partial chunks and one-token chunks; stale slots and free
 blocks hold NaN, so any read past a sequence's context shows."""
 import dataclasses
+import math
 
 import numpy as np
 import pytest
@@ -300,3 +301,48 @@ def test_prefill_e4m3_recompute_matches_decode():
     assert _err(out, ref) <= TOL["e4m3"]
     assert _err(dec, ref[last.numpy()]) <= TOL["e4m3"]
     assert float((out[last.cuda()].float() - dec.float()).abs().max()) <= 2 * TOL["e4m3"]
+
+
+def test_prefill_fp8_recompute_after_quantise_on_write():
+    """The FP8 workload's recompute path end to end: a victim's retained history (bf16 K/V) is
+    quantised into an E4M3 cache by pa_write_kv_fp8 at fresh, scattered slots, prefilled over
+    that cache by pa_prefill, and its next step decoded by pa_decode; both equal the oracle
+    run on the bytes the kernel wrote (and the write equals the oracle's quantise-on-write)."""
+    g = torch.Generator().manual_seed(12)
+    hq, hkv, d, B, L = 32, 8, 128, 16, 700
+    nblk = 200
+    k = torch.randn(L, hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(L, hkv, d, generator=g).to(torch.bfloat16)
+    ks, vs = float(k.float().abs().max()) / 448.0, float(v.float().abs().max()) / 448.0
+    table = torch.randperm(nblk, generator=g)[: (L + B - 1) // B].to(torch.int32)
+    pos = torch.arange(L)
+    slots = (table[pos // B].long() * B + pos % B).to(torch.int64)
+    kp = torch.full((nblk, hkv, B, d), 0x7F, dtype=torch.uint8)  # stale bytes: E4M3 NaN
+    vp = kp.clone()
+    exp_k, exp_v = kp.numpy().copy(), vp.numpy().copy()
+    orc = oracle.load()
+    assert orc.write_kv_fp8(k, v, exp_k, exp_v, slots, src_dtype="bf16", num_kv_heads=hkv,
+                            head_dim=d, block_size=B, k_scale=ks, v_scale=vs) == 0
+    gk, gv = kp.cuda(), vp.cuda()
+    pa.pa_write_kv_fp8(k.cuda(), v.cuda(), gk, gv, slots.cuda(), ks, vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(gk.cpu().numpy(), exp_k) and np.array_equal(gv.cpu().numpy(), exp_v)
+    bt = torch.full((1, 64), -1, dtype=torch.int32)
+    bt[0, : table.numel()] = table
+    cl = torch.tensor([L], dtype=torch.int32)
+    qs = torch.tensor([0, L], dtype=torch.int32)
+    q = torch.randn(L, hq, d, generator=g).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(d)
+    ref = orc.prefill(q, torch.from_numpy(exp_k), torch.from_numpy(exp_v), bt, cl, qs,
+                      dtype="e4m3", q_dtype="bf16", num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                      block_size=B, scale=scale, k_scale=ks, v_scale=vs)
+    out = pa.pa_prefill(q.cuda(), gk, gv, bt.cuda(), cl.cuda(), qs.cuda(), scale, k_scale=ks,
+                        v_scale=vs)
+    qd = torch.randn(1, hq, d, generator=g).to(torch.bfloat16)
+    dec_ref = orc.decode(qd, torch.from_numpy(exp_k), torch.from_numpy(exp_v), bt, cl,
+                         q_dtype="bf16", kv_dtype="e4m3", num_q_heads=hq, num_kv_heads=hkv,
+                         head_dim=d, block_size=B, scale=scale, k_scale=ks, v_scale=vs)
+    dec = pa.pa_decode(qd.cuda(), gk, gv, bt.cuda(), cl.cuda(), scale, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert _err(out, ref) <= TOL["e4m3"]
+    assert _err(dec, dec_ref) <= TOL["e4m3"]
