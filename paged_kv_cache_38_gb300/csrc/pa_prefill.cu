@@ -31,8 +31,14 @@
 //     item's epilogue (O divided by the row sums, rows stored) runs inside the next item's
 //     first tile, once that tile's P is written, so that the wait for the item's last PV
 //     overlaps the next tile's softmax.
-// Every wait is bounded; on a timeout the CTA flags PA_ERR_TIMEOUT, the roles wind down, the
-// MMAs drain through one last commit and the tensor memory is freed before the CTA returns.
+// An E4M3 cache (head_dim 128) goes through the same pipeline on f16 MMAs: each K/V copy brings
+// the tile's raw bytes into the upper half of its stage and the whole producer warp widens them
+// to f16 in place (exact); the query-loader warp moves bf16 query rows to f16, each with a
+// power-of-two scale that the softmax folds into its score scale; v_scale joins the epilogue.
+// Every wait is bounded (pa_testing_set_wait_limit can shorten the waits of one role on another
+// and make one CTA's MMA issuer stop, for tests); on a timeout the CTA flags PA_ERR_TIMEOUT, the
+// roles wind down, the copies and MMAs in flight drain (those waits keep a one-second limit)
+// and the tensor memory is freed before the CTA returns.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
