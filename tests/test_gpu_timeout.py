@@ -91,31 +91,6 @@ def test_decode_grid_barrier_wait_expires(name):
     assert torch.equal(out, res)
 
 
-def test_decode_item_waits_expire_anywhere():
-    """A limit of 1 ns makes any wait that is not met at once give up, wherever it is (the
-    scheduler's, producers' and consumers' mbarrier waits, the grid barrier). Whether and where
-    a launch gives up depends on timing; every launch must still return with its copies drained
-    and leave the next call correct."""
-    spec = synth.SPECS["fp8_long"].scaled(num_seqs=24, ctx_range=(100, 3000))
-    case = synth.make_case(spec, seed=82).to("cuda")
-    ref = oracle_decode(case)
-    ws = torch.zeros(1 << 26, dtype=torch.uint8, device="cuda")  # 47 splits of 64 tokens
-    out = torch.empty_like(case.q)
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pa.pa_testing_set_wait_limit(1, -1)
-    for _ in range(5):
-        _decode(case, ws, out, err)
-    torch.cuda.synchronize()
-    assert int(err.item()) & ~pa.PA_ERR_TIMEOUT == 0
-    assert int(ws[:24].count_nonzero().item()) == 0
-    pa.pa_testing_set_wait_limit(0, -1)
-    err.zero_()
-    res = _decode(case, ws, out, err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    assert max_abs_err(res, ref) <= TOL["e4m3"]
-
-
 def _prefill_case():
     spec = synth.DecodeSpec("pf_timeout", 6, 32, 8, 128, 16, "bf16", "bf16", ctx_range=(200, 900))
     case = synth.make_case(spec, seed=83)
@@ -152,23 +127,6 @@ def test_prefill_waits_expire_when_mma_issuer_stalls():
         torch.cuda.synchronize()
         assert time.perf_counter() - t0 < FAST_S
         assert int(err.item()) & pa.PA_ERR_TIMEOUT
-    pa.pa_testing_set_wait_limit(0, -1)
-    err.zero_()
-    out = _prefill(g, qs, q, err)
-    torch.cuda.synchronize()
-    assert int(err.item()) == 0
-    assert _prefill_err(out, ref) <= TOL["bf16"]
-
-
-def test_prefill_waits_expire_anywhere():
-    """A 1 ns limit on the prefill roles' waits (see the decode case above)."""
-    g, qs, q, ref = _prefill_case()
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pa.pa_testing_set_wait_limit(1, -1)
-    for _ in range(5):
-        _prefill(g, qs, q, err)
-    torch.cuda.synchronize()
-    assert int(err.item()) & ~pa.PA_ERR_TIMEOUT == 0
     pa.pa_testing_set_wait_limit(0, -1)
     err.zero_()
     out = _prefill(g, qs, q, err)
