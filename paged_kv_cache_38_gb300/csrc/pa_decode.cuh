@@ -197,9 +197,19 @@ struct Consumer<KV, D, G, false> {
     }
   }
 
-  // One 16-token tile: rows r0..r0+15 of the stage, `valid` = bit mask of usable tokens.
+  // One 16-token tile: rows r0..r0+15 of the stage, `valid` = bit mask of usable tokens. A full
+  // tile (every token valid, all but an item's last tile) skips the per-row validity tests.
   __device__ void tile(const DecodeParams& p, uint32_t ks, uint32_t vs, int r0, uint32_t valid,
                        float score_scale) {
+    if (valid == 0xffffu)
+      tile_impl<true>(p, ks, vs, r0, valid, score_scale);
+    else
+      tile_impl<false>(p, ks, vs, r0, valid, score_scale);
+  }
+
+  template <bool kFull>
+  __device__ __forceinline__ void tile_impl(const DecodeParams& p, uint32_t ks, uint32_t vs, int r0,
+                                            uint32_t valid, float score_scale) {
     float s[kIters][G];
 #pragma unroll
     for (int it = 0; it < kIters; ++it) {
@@ -214,7 +224,7 @@ struct Consumer<KV, D, G, false> {
         for (int e = 0; e < kE; ++e) dot = fmaf(q[h][e], k[e], dot);
 #pragma unroll
         for (int off = 1; off < kCpr; off <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        s[it][h] = ((valid >> r) & 1u) ? dot * score_scale : -INFINITY;
+        s[it][h] = (kFull || ((valid >> r) & 1u)) ? dot * score_scale : -INFINITY;
       }
     }
     float ref[G];
@@ -236,7 +246,7 @@ struct Consumer<KV, D, G, false> {
 #pragma unroll
     for (int it = 0; it < kIters; ++it) {
       const int r = it * kGroups + grp;
-      if (!((valid >> r) & 1u)) continue;
+      if (!kFull && !((valid >> r) & 1u)) continue;
       const StageRow row = stage_row(r0 + r, p.log2_srows, Gm::kRegions, p.region_stride);
       float v[kE];
       load_row(chunk_addr(vs, row, ci, p.region_stride), v);
@@ -345,7 +355,19 @@ struct Consumer<KV, D, G, true> {
     }
   }
 
+  // A full tile (every token valid, all but an item's last tile) skips the validity selects and
+  // masks: on the E4M3 path they were a tenth of the integer-pipe work.
   __device__ void tile(const DecodeParams& p, uint32_t ks, uint32_t vs, int r0, uint32_t valid,
+                       float score_scale) {
+    if (valid == 0xffffu)
+      tile_impl<true>(p, ks, vs, r0, valid, score_scale);
+    else
+      tile_impl<false>(p, ks, vs, r0, valid, score_scale);
+  }
+
+  template <bool kFull>
+  __device__ __forceinline__ void tile_impl(const DecodeParams& p, uint32_t ks, uint32_t vs, int r0,
+                                            uint32_t valid,
                        float score_scale) {
     const int lane = (t4 | (g << 2));
     float s[kNT][4];
@@ -392,7 +414,7 @@ struct Consumer<KV, D, G, true> {
     }
 
     // ---- online softmax over the tile's 16 tokens (rows g, g+8), heads 2*t4 + {0,1}
-    const bool ok_lo = (valid >> g) & 1u, ok_hi = (valid >> (g + 8)) & 1u;
+    const bool ok_lo = kFull || ((valid >> g) & 1u), ok_hi = kFull || ((valid >> (g + 8)) & 1u);
     uint32_t pb[kNT][2][kSplitP ? 2 : 1];
 #pragma unroll
     for (int nt = 0; nt < kNT; ++nt) {
@@ -437,7 +459,7 @@ struct Consumer<KV, D, G, true> {
 
     // masks of the value rows this lane feeds: tokens (2t4, 2t4+1) and (2t4+8, 2t4+9)
     uint32_t mask01 = 0xffffffffu, mask23 = 0xffffffffu;
-    if (valid != 0xffffu) {
+    if (!kFull && valid != 0xffffu) {
       mask01 = (((valid >> (2 * t4)) & 1u) ? 0x0000ffffu : 0u) |
                (((valid >> (2 * t4 + 1)) & 1u) ? 0xffff0000u : 0u);
       mask23 = (((valid >> (2 * t4 + 8)) & 1u) ? 0x0000ffffu : 0u) |
@@ -462,10 +484,14 @@ struct Consumer<KV, D, G, true> {
         for (int w = 0; w < 4; ++w) {
           const uint32_t lo = prmt(xa[w], ya[w], 0x5140u);
           const uint32_t hi = prmt(xa[w], ya[w], 0x7362u);
-          va[pair][4 * w + 0] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo & 0xffffu)) & msk;
-          va[pair][4 * w + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo >> 16)) & msk;
-          va[pair][4 * w + 2] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi & 0xffffu)) & msk;
-          va[pair][4 * w + 3] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi >> 16)) & msk;
+          va[pair][4 * w + 0] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo & 0xffffu));
+          va[pair][4 * w + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(lo >> 16));
+          va[pair][4 * w + 2] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi & 0xffffu));
+          va[pair][4 * w + 3] = e4m3x2_to_f16x2(static_cast<uint16_t>(hi >> 16));
+          if constexpr (!kFull) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) va[pair][4 * w + e] &= msk;
+          }
         }
       }
 #pragma unroll
@@ -483,10 +509,12 @@ struct Consumer<KV, D, G, true> {
       for (int j = 0; j < kK; ++j) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(chunk_addr(vs, row, 2 * j + (i & 1), p.region_stride), a0, a1, a2, a3);
-        a0 &= mask01;
-        a1 &= mask01;
-        a2 &= mask23;
-        a3 &= mask23;
+        if constexpr (!kFull) {
+          a0 &= mask01;
+          a1 &= mask01;
+          a2 &= mask23;
+          a3 &= mask23;
+        }
 #pragma unroll
         for (int nt = 0; nt < kNT; ++nt) {
           mma_16816<kBF16>(o[nt][j], a0, a1, a2, a3, pb[nt][0][0], pb[nt][1][0]);
