@@ -6,7 +6,7 @@
 // together). Query i of a chunk of n tokens over a cache of L positions stands at position
 // L - n + i and attends to positions 0 .. L - n + i.
 //
-// GB300 design: a persistent kernel, two CTAs per SM (about 113 KB of shared memory and 256
+// GB300 design: a persistent kernel, two CTAs per SM (about 97 KB of shared memory and 256
 // tensor-memory columns each at head_dim 128, so the two overlap each other's softmax and MMA
 // phases). A work item is one tile of 128 query rows of one (sequence, kv head); a row is one
 // (token, query head of the group), so a tile holds 128 / G tokens and the GQA group shares
@@ -22,15 +22,16 @@
 //     2-stage ring;
 //   * warp 1 allocates tensor memory and one lane issues the MMAs: S_j = Q K_j^T (M 128, N 64)
 //     into one of two TMEM S buffers, and O += P_j V_j (M 128, N = head_dim) into the TMEM O
-//     accumulator, PV first when both are ready; one tcgen05.commit per MMA group signals its
-//     completion on an mbarrier, which also hands the group's K (or V) stage back to its
-//     producer;
+//     accumulator with P_j read from tensor memory, PV first when both are ready; one
+//     tcgen05.commit per MMA group signals its completion on an mbarrier, which also hands the
+//     group's K (or V) stage back to its producer;
 //   * warps 4-7 (one thread per row) read S with tcgen05.ld, apply the causal mask and the
-//     online softmax (log2 domain, packed fp32 pairs), write P (16-bit, swizzled K-major) to
-//     shared memory and rescale O in tensor memory when a row's running maximum grows; an
-//     item's epilogue (O divided by the row sums, rows stored) runs inside the next item's
-//     first tile, once that tile's P is written, so that the wait for the item's last PV
-//     overlaps the next tile's softmax.
+//     online softmax (log2 domain, packed fp32 pairs), write P (16-bit pairs) with tcgen05.st
+//     over the first half of the S buffer it came from, and rescale O in tensor memory when a
+//     row's running maximum grows. P_j thus never waits for PV_{j-1}; only a rescale and the
+//     item epilogue read O. An item's epilogue (O divided by the row sums, rows stored) runs
+//     inside the next item's first tile, once that tile's P is written, so that the wait for
+//     the item's last PV overlaps the next tile's softmax.
 // An E4M3 cache (head_dim 128) goes through the same pipeline on f16 MMAs: each K/V copy brings
 // the tile's raw bytes into the upper half of its stage and the whole producer warp widens them
 // to f16 in place (exact); the query-loader warp moves bf16 query rows to f16, each with a
@@ -169,12 +170,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   }
   const uint32_t sQ = base;
   const uint32_t sKV = sQ + kRegions * kQRegion;  // stage st: K at sKV + 2 st kKVBytes, V after it
-  const uint32_t sP = sKV + kPfStages * 2 * kKVBytes;
-  uint8_t* ctl = bp + (sP - base) + kPfRows * 128;
+  uint8_t* ctl = bp + (sKV + kPfStages * 2 * kKVBytes - base);
   // K and V stream through separate rings: K of tile j is free once S_j is computed, V once
   // PV_j is, so K loads run a whole softmax ahead of V loads. Every phase below counts tiles
   // (or items) over the whole run of the CTA. Tile j uses stage j % 2 of both rings, S buffer
-  // j % 2 and completion barriers s_full[j % 2] and o_done[j % 2]; with one commit per MMA
+  // j % 2 (whose first 32 columns then take P_j, read by PV_j from tensor memory), barriers
+  // p_full[j % 2] and completion barriers s_full[j % 2] and o_done[j % 2]; with one commit per MMA
   // group (a second one per group slows the MMA stream by about a tenth), those two barriers
   // also release the stage's K and V to the producers (each producer waits on every phase of
   // its own stage, so a parity wait cannot pass on a phase that is still one behind). The query
@@ -184,9 +185,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   uint64_t* k_full = reinterpret_cast<uint64_t*>(ctl);  // [kPfStages]
   uint64_t* v_full = k_full + kPfStages;                 // [kPfStages]
   uint64_t* s_full = v_full + kPfStages;                 // [2] S_j complete: K_j free too
-  uint64_t* s_free = s_full + 2;                         // [2]
-  uint64_t* p_full = s_free + 2;
-  uint64_t* o_done = p_full + 1;                         // [2] PV_j complete: V_j free too
+  uint64_t* p_full = s_full + 2;                         // [2] P_j written (4 warps)
+  uint64_t* o_done = p_full + 2;                         // [2] PV_j complete: V_j and S buffer free
   uint64_t* o_free = o_done + 2;                         // O read by the epilogue (4 warps)
   uint64_t* q_full = o_free + 1;                         // the item's query tile landed
   uint64_t* q_empty = q_full + 1;                        // the item's last S complete
@@ -213,10 +213,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(s_full + i), 1);
-      mbar_init(smem_addr(s_free + i), 4);
+      mbar_init(smem_addr(p_full + i), 4);
       mbar_init(smem_addr(o_done + i), 1);
     }
-    mbar_init(smem_addr(p_full), 4);
     mbar_init(smem_addr(o_free), 4);
     mbar_init(smem_addr(q_full), 1);
     mbar_init(smem_addr(q_empty), 1);
@@ -520,14 +519,15 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       // attention sequence ran at half the pipe's rate.
       const uint64_t dQ = umma_sdesc(sQ, 16, 1024);
       const uint64_t dK = umma_sdesc(sKV, 16, 1024);
-      const uint64_t dP = umma_sdesc(sP, 16, 1024);
       const uint64_t dV = umma_sdesc(sKV + kKVBytes, kKVRegion, 1024);
       constexpr uint32_t idO = umma_idesc_f16(kPfRows, D, BF16, true);
       // Two cursors over the items: S_ns is issued as soon as K_ns has landed (and its S buffer
       // is free, and at an item's first tile its queries have landed), PV_npv as soon as P_npv
       // and V_npv are ready (and, at an item's first tile, once the epilogue has read O),
       // whichever comes first, PV before S when both are. S runs ahead of PV by up to two
-      // tiles, across item boundaries.
+      // tiles, across item boundaries. S buffer b is free once the PV that read P from it two
+      // tiles earlier has completed: tcgen05 orders MMAs of one thread only when they share an
+      // accumulator, so issuing S after that PV would not be enough.
       int kS = 0, jS = 0, ns = 0;   // S stream: item, tile in item, S issued over all items
       bool haveS = false, endS = false;
       PfItem iS{};
@@ -558,14 +558,15 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         }
         if (haveP && npv < ns && !stalled) {
           const int stp = npv % kPfStages;
-          if (mbar_test(smem_addr(p_full), npv & 1) &&
+          if (mbar_test(smem_addr(p_full + stp), (npv >> 1) & 1) &&
               mbar_test(smem_addr(v_full + stp), (npv / kPfStages) & 1) &&
               (jP > 0 || nO == 0 || mbar_test(smem_addr(o_free), (nO - 1) & 1))) {
             tc_fence_after();
             const uint64_t dVs = dV + ((2u * stp * kKVBytes) >> 4);
+            const uint32_t tP = tS + 64 * stp;
 #pragma unroll
             for (int k = 0; k < kPfKeys / 16; ++k)
-              umma_f16(tO, dP + k * 2, dVs + k * 128, idO, jP > 0 || k > 0);
+              umma_f16_ta(tO, tP + 8 * k, dVs + k * 128, idO, jP > 0 || k > 0);
             umma_commit(smem_addr(o_done + stp));
             ++npv;
             if (++jP == iP.ntiles) {
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         if (haveS && !(stalled && ns >= 1)) {
           const int st = ns % kPfStages, b = ns & 1;
           if (mbar_test(smem_addr(k_full + st), (ns / kPfStages) & 1) &&
-              (ns < 2 || mbar_test(smem_addr(s_free + b), ((ns >> 1) - 1) & 1)) &&
+              (ns < 2 || mbar_test(smem_addr(o_done + b), ((ns >> 1) - 1) & 1)) &&
               (jS > 0 || (kFp8 ? mbar_test(smem_addr(q_ready + kS % kSlots), (kS / kSlots) & 1)
                                 : mbar_test(smem_addr(q_full), kS & 1)))) {
             tc_fence_after();
@@ -722,9 +723,6 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             x[32 + i] = __uint_as_float(r1[i]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(s_free + b));
 
         const int key0 = j * kPfKeys;
         // Rows that see all 64 keys of the tile (every tile before the diagonal) need no mask.
@@ -789,7 +787,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         l = l * alpha + psum;
         m = m_new;
 
-        if (jx >= 1) {  // PV of the previous tile done: O is stable and the P buffer free
+        // P_j goes to its own S buffer, so only reading or rescaling O waits for PV_{j-1}: the
+        // previous item's epilogue (at an item's first tile) and a rescale (rare)
+        const bool rescale = j >= 1 && __any_sync(0xffffffffu, alpha != 1.f);
+        const bool epi = j == 0 && pend;
+        if (rescale || epi) {
           ok = mbar_wait_bounded(smem_addr(o_done + ((jx - 1) & 1)), ((jx - 1) >> 1) & 1, p.wait_ns);
           if (__any_sync(0xffffffffu, !ok)) {
             ok = false;
@@ -797,6 +799,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           }
           tc_fence_after();
         }
+        bool zeroed = false;
         if (j == it.ntiles - 1 && key0 + kPfKeys > it.L) {
           // value rows past the cache's last position (stale slots, or not loaded) become zero,
           // so that zero weights cannot meet a NaN; the tile's V copies must have landed first
@@ -814,15 +817,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             *reinterpret_cast<uint4*>(bp + (vst - base) + (c / 8) * kKVRegion + row * 128 +
                                       (c % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
+          zeroed = true;
         }
-        // P row r, swizzled K-major: 16-byte chunk c holds keys 8c .. 8c + 7
-        uint8_t* prow = bp + (sP - base);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(prow + sw128_offset(r, c)) =
-              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        if (j == 0 && pend) epilogue();  // the previous item's O is complete (waited above)
-        if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // P row r into the first 32 columns of S buffer b (S_j has been read)
+        tmem_st32_nowait(tS + 64 * b + lane_base, pk);
+        if (epi) epilogue();  // the previous item's O is complete (waited above)
+        if (rescale) {
 #pragma unroll 1
           for (int c = 0; c < D; c += 16) {
             float v[16];
@@ -832,10 +832,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             tmem_st16(tO + lane_base + c, v);
           }
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
+        if (zeroed) fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(p_full));
+        if (lane == 0) mbar_arrive(smem_addr(p_full + b));
       }
       if (!ok) break;
       // ---- the item's epilogue is deferred (see above)
@@ -1026,7 +1027,7 @@ pa_status run_prefill(const pa_prefill_args& a, cudaStream_t stream, std::string
   // no alignment slack: the kernel needs (and checks) a 1024-byte aligned dynamic region, and
   // two CTAs then fit on an SM
   const size_t smem = regions * kPfRows * 128 + kPfStages * 2 * regions * kPfKeys * 128 +
-                      kPfRows * 128 + (fp8 ? kCtlBytesFp8 : kCtlBytes);
+                      (fp8 ? kCtlBytesFp8 : kCtlBytes);
   const int sms = device_sm_count();
   if (sms <= 0) {
     msg = "cannot read the SM count of the current device";
