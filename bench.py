@@ -736,7 +736,17 @@ def run_quantise_bench(dev, flush, peaks) -> dict:
     res = {"tokens": ntok, "bytes": byts, "ms": round(t, 4), "gbs": round(gbs, 1),
            "pct_of_peak": round(100 * gbs / peaks["hbm_gbs"], 1),
            "step_256_tokens_us": round(t_small * 1e3, 2)}
-    del k, v, kp, vp
+    # the same tokens through pa_write_kv into a bf16 pool (what a prefill writes without FP8)
+    kp16 = torch.empty(nblk, hkv, b, d, dtype=torch.bfloat16, device=dev)
+    vp16 = torch.empty_like(kp16)
+    call16 = lambda: pa.pa_write_kv(k, v, kp16, vp16, slots)  # noqa: E731
+    call16()
+    t16 = statistics.mean(time_steps(call16, 10, flush))
+    byts16 = ntok * (2 * hkv * d * 2 * 2 + 8)  # bf16 read and written, slot read
+    res["bf16_write_kv"] = {"bytes": byts16, "ms": round(t16, 4),
+                            "gbs": round(byts16 / (t16 * 1e-3) / 1e9, 1),
+                            "pct_of_peak": round(100 * byts16 / (t16 * 1e-3) / 1e9 / peaks["hbm_gbs"], 1)}
+    del k, v, kp, vp, kp16, vp16
     torch.cuda.empty_cache()
     return res
 
@@ -966,19 +976,24 @@ def main():
                     help="time budget of the reference arm's warm-up and timed steps")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill benches and print their result")
+    ap.add_argument("--quantise-only", action="store_true",
+                    help="run only the 32,768-token pa_write_kv_fp8 / pa_write_kv bench and print "
+                         "its result (a small case for profiling)")
     ap.add_argument("--copy-only-layers", type=int, default=0,
                     help="run only the 4,096-pair pa_copy_blocks bench with this many layers "
                          "(a small case for profiling) and print its result")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.copy_only_layers > 0 or args.prefill_only:
+    if args.copy_only_layers > 0 or args.prefill_only or args.quantise_only:
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
         if args.prefill_only:
             print(json.dumps(run_prefill_bench(dev, flush, load_peaks())))
+        elif args.quantise_only:
+            print(json.dumps(run_quantise_bench(dev, flush, load_peaks())))
         else:
             print(json.dumps(run_copy_bench(dev, flush, load_peaks(), layers=args.copy_only_layers)))
         return
