@@ -976,6 +976,9 @@ def main():
                     help="time budget of the reference arm's warm-up and timed steps")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill benches and print their result")
+    ap.add_argument("--swap-only", action="store_true",
+                    help="run only the 188 MiB preemption swap bench and print its result "
+                         "(a small case for profiling)")
     ap.add_argument("--quantise-only", action="store_true",
                     help="run only the 32,768-token pa_write_kv_fp8 / pa_write_kv bench and print "
                          "its result (a small case for profiling)")
@@ -985,7 +988,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.copy_only_layers > 0 or args.prefill_only or args.quantise_only:
+    if args.copy_only_layers > 0 or args.prefill_only or args.quantise_only or args.swap_only:
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
         l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -994,6 +997,8 @@ def main():
             print(json.dumps(run_prefill_bench(dev, flush, load_peaks())))
         elif args.quantise_only:
             print(json.dumps(run_quantise_bench(dev, flush, load_peaks())))
+        elif args.swap_only:
+            print(json.dumps(run_swap_bench(dev)))
         else:
             print(json.dumps(run_copy_bench(dev, flush, load_peaks(), layers=args.copy_only_layers)))
         return
