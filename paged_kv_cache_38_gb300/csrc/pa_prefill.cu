@@ -636,8 +636,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     bool ok = true;
     // An item's epilogue (O / l to its rows, then O and the item slot released) is deferred
     // into the next item's first tile, after that tile's weights are computed and its P is
-    // written: the wait for the item's last PV then overlaps useful work. O is complete there,
-    // since the wait for PV_{j-1} before writing P is the previous item's last PV.
+    // written: the wait for the item's last PV (PV_{j-1} of that tile, waited for just before)
+    // then overlaps useful work.
     bool pend = false, pend_valid = false;
     float pend_inv = 0.f;
     uint4* pend_dst = nullptr;
