@@ -101,7 +101,8 @@ typedef enum {
  *   workspace    >= pa_decode_workspace_size(args) bytes, 256-byte aligned, contents ignored
  * Supported: head_dim in {64, 128}; block_size in {4, 8, 16, 32, 64}; group size
  * num_q_heads/num_kv_heads in {1, 2, 4, 8, 16}; (q, kv) dtype pairs (F16, F16), (BF16, BF16),
- * (F16, FP8_E4M3), (BF16, FP8_E4M3). k_scale / v_scale multiply the stored values (use 1.0
+ * (F16, FP8_E4M3), (BF16, FP8_E4M3), the E4M3 pairs at head_dim 128 only (PA_EUNSUPPORTED
+ * otherwise). k_scale / v_scale multiply the stored values (use 1.0
  * for 16-bit KV). Work is split along the context ("split-K") when that improves occupancy;
  * split_tokens = 0 lets the library choose, otherwise it must be a multiple of max(16, B).
  */

@@ -268,9 +268,11 @@ def make_case(spec: DecodeSpec, seed: int, *, device="cpu", logical: bool = True
                 vs = torch.cat([group_prompt[g][1], vs])
             k32.append(ks)
             v32.append(vs)
-        if spec.kv_dtype == "e4m3":
-            k_scale = float(max(t.abs().max() for t in k32)) / E4M3_MAX
-            v_scale = float(max(t.abs().max() for t in v32)) / E4M3_MAX
+        if spec.kv_dtype == "e4m3":  # empty contexts hold no values: scale 1 if all are empty
+            k_scale = max((float(t.abs().max()) for t in k32 if t.numel()),
+                          default=E4M3_MAX) / E4M3_MAX
+            v_scale = max((float(t.abs().max()) for t in v32 if t.numel()),
+                          default=E4M3_MAX) / E4M3_MAX
         k_log = [_cast(t, spec.kv_dtype, k_scale) for t in k32]
         v_log = [_cast(t, spec.kv_dtype, v_scale) for t in v32]
         kp = _poison_fill(shape, spec.kv_dtype, device) if poison else \
