@@ -104,7 +104,9 @@ typedef enum {
  * (F16, FP8_E4M3), (BF16, FP8_E4M3), the E4M3 pairs at head_dim 128 only (PA_EUNSUPPORTED
  * otherwise). k_scale / v_scale multiply the stored values (use 1.0
  * for 16-bit KV). Work is split along the context ("split-K") when that improves occupancy;
- * split_tokens = 0 lets the library choose, otherwise it must be a multiple of max(16, B).
+ * split_tokens = 0 lets the library choose, otherwise it must be a multiple of max(16, B) and
+ * split_tokens / min(B, 16) (min(B, 32) for an E4M3 cache) must be below 256 (PA_EINVAL
+ * otherwise).
  */
 typedef struct pa_decode_args {
   const void* q;

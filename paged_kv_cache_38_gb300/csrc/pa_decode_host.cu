@@ -219,6 +219,9 @@ pa_status plan_decode(const pa_decode_args& a, int sm_count, DecodePlan& pl, std
     const int sms = sm_count > 0 ? sm_count : 148;
     while (tokens > 4 * stok && units * ((a.max_ctx_len + tokens - 1) / tokens) < 8LL * sms)
       tokens /= 2;
+    // a work item's table slice holds at most kMaxItemUnits copy units (small blocks of a
+    // 1-byte cache would exceed it at 2048 tokens)
+    while (tokens > stok && tokens / pl.stage_rows + 1 > kMaxItemUnits) tokens /= 2;
     pl.split_tokens = std::max(stok, (tokens / stok) * stok);
   }
   pl.max_splits = std::max(1, (a.max_ctx_len + pl.split_tokens - 1) / pl.split_tokens);

@@ -55,6 +55,25 @@ def test_decode_matches_oracle(spec, split):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("B,nseq", [(4, 100), (8, 160)])
+def test_decode_e4m3_small_blocks_automatic_split(B, nseq):
+    """An E4M3 cache of 4- or 8-token blocks with the automatic split: enough work that the
+    planner would keep 2048 (or 1024) tokens per work item, more copy units than one item's
+    table slice holds; it halves the split instead of refusing its own plan. An explicit split
+    past that bound is refused (PA_EINVAL), as pa.h states."""
+    spec = synth.DecodeSpec(f"e4m3_b{B}_auto", nseq, 8, 8, 128, B, "e4m3", "bf16",
+                            ctx_range=(1000, 2000))
+    case = synth.make_case(spec, seed=B).to("cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = gpu_decode(case, split_tokens=0, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert max_abs_err(out, oracle_decode(case)) <= TOL["e4m3"]
+    with pytest.raises(pa.PaError) as e:
+        gpu_decode(case, split_tokens=256 * B)
+    assert e.value.status == pa.PA_EINVAL
+
+
 def test_decode_edge_lengths():
     """Empty, single-token, block-boundary and full-capacity contexts, NaN in stale slots."""
     for B in (4, 8, 16, 32, 64):
