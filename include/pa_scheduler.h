@@ -100,7 +100,9 @@ void pa_scheduler_destroy(pa_scheduler* s);
 /* Queue a request of prompt_len tokens that produces max_new_tokens tokens in each of
  * num_samples samples (1..256) sharing the prompt. PA_EINVAL for a repeated id, sizes < 1, or
  * a request that could never fit (ceil((prompt_len + max_new_tokens) / block_size) above
- * max_blocks_per_seq, or that many blocks per sample above the pool). */
+ * max_blocks_per_seq, that many blocks per sample above the pool, or more samples than
+ * max_running_seqs: admission stops at the first waiting group that does not fit, so such a
+ * group would hold every request behind it). */
 pa_status pa_scheduler_add_request(pa_scheduler* s, int64_t request_id, int32_t prompt_len,
                                    int32_t max_new_tokens, int32_t num_samples);
 

@@ -109,8 +109,8 @@ class Scheduler:
                     num_samples: int) -> bool:
         if request_id in self.requests or prompt_len < 1 or max_new_tokens < 1:
             return False
-        if not 1 <= num_samples <= 256:
-            return False
+        if not 1 <= num_samples <= min(256, self.max_running):
+            return False  # a group larger than max_running_seqs could never be admitted
         longest = prompt_len + max_new_tokens
         if -(-longest // self.B) > self.max_blocks:
             return False

@@ -341,6 +341,10 @@ pa_status pa_scheduler_add_request(pa_scheduler* s, int64_t request_id, int32_t 
   if (s->groups.count(request_id) || prompt_len < 1 || max_new_tokens < 1 || num_samples < 1 ||
       num_samples > 256)
     return pa::record_error(PA_EINVAL, "repeated request id, or a size out of range");
+  // admission takes whole groups within max_running_seqs: a larger group could never run, and
+  // would hold every request queued behind it
+  if (num_samples > s->max_running)
+    return pa::record_error(PA_EINVAL, "more samples than max_running_seqs");
   const int64_t longest = ceil_div(static_cast<int64_t>(prompt_len) + max_new_tokens, s->block_size);
   if (longest > s->max_blocks || longest * num_samples > s->num_blocks)
     return pa::record_error(PA_EINVAL, "the request can never fit the pool or a block table");

@@ -114,8 +114,9 @@ class Replay:
 
     def apply(self, plan, max_new: dict):
         B = self.B
-        # preemption: the newest running group goes, with all of its blocks
-        before = list(self.running)
+        # preemption: the newest running group goes, with all of its blocks (the step retires
+        # finished groups first, so they no longer count as running)
+        before = [r for r in self.running if r not in plan.finished]
         for r in plan.preempted:
             assert r in before, "only running groups are preempted"
             assert all(self.arrival[r] >= self.arrival[x] for x in before if x != r), \
@@ -236,4 +237,24 @@ def pin_preemption_happens(bm):
     assert all(v > 0 for v in seen.values()), seen
 
 
-ALL_PINS = [pin_figures_1_5, pin_replay_recompute, pin_replay_swap, pin_preemption_happens]
+def pin_oversized_group_refused(bm):
+    """Admission takes whole groups, in queue order, within max_running_seqs ("Continuous
+    Batching and PagedAttention", the scheduler loop: admit while memory permits; the summary
+    page: all sequences of a group are scheduled together). A group with more samples than that
+    could never run and, first in the queue, would hold every request behind it: it is refused
+    when added, and the requests after it all finish."""
+    for mode in (bm.RECOMPUTE, bm.SWAP):
+        s = bm.Scheduler(64, 4, 16, 3, mode, 64)
+        assert s.add_request(0, 5, 3, 1)
+        assert not s.add_request(1, 5, 3, 4), "a group larger than max_running_seqs"
+        assert s.add_request(2, 5, 3, 3), "a group of exactly max_running_seqs"
+        assert s.add_request(3, 6, 2, 1)
+        for _ in range(100):
+            s.step()
+            if not s.has_unfinished():
+                break
+        assert not s.has_unfinished(), "every admitted request finishes"
+
+
+ALL_PINS = [pin_figures_1_5, pin_replay_recompute, pin_replay_swap, pin_preemption_happens,
+            pin_oversized_group_refused]

@@ -35,6 +35,8 @@ MUTANTS = [
     ("append_slot_off_by_one", "writes.append((s, s.length, b * self.B + s.length % self.B))",
      "writes.append((s, s.length, b * self.B + (s.length + 1) % self.B))"),
     ("waiting_back_of_queue", "self.waiting.appendleft(victim)", "self.waiting.append(victim)"),
+    ("oversized_group_accepted", "if not 1 <= num_samples <= min(256, self.max_running):",
+     "if not 1 <= num_samples <= 256:"),
 ]
 
 
